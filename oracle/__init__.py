@@ -1,0 +1,188 @@
+"""fp64 CPU oracle for exact scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the CPU-baseline
+leg of ``bench.py`` use it. The product path never imports this package, and
+this package never imports the product package; the two share only the seeded
+input generators, which hold none of the method's arithmetic.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, pthreads); this
+module compiles it with gcc and marshals numpy arrays to it. Every function
+takes and returns float64 arrays laid out ``[B, H, N, d]`` (statistics
+``[B, H, N]``).
+
+What is computed, and which passage of the pages each part follows, is stated
+at the top of ``attn_oracle.c``. Parity status: every entry point is pinned by
+``tests/test_oracle_*.py`` (worked examples printed on the pages, closed forms,
+invariants, brute force and finite differences).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into oracle/_build/liboracle.so (gcc, -O2, IEEE)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+             "-fno-fast-math", "-ffp-contract=off", "-Wall", "-Wextra",
+             "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int)
+            up = ctypes.POINTER(ctypes.c_ubyte)
+            i = ctypes.c_int
+            lib.oracle_forward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double,
+                                           up, i, ip, i, i]
+            lib.oracle_forward.restype = i
+            lib.oracle_forward_tiled.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i,
+                                                 ctypes.c_double, up, i, i, i, i]
+            lib.oracle_forward_tiled.restype = i
+            lib.oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i,
+                                            ctypes.c_double, up, i, ip, i, ip, i, i]
+            lib.oracle_backward.restype = i
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _f64(x, name):
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if a.ndim != 4:
+        raise ValueError(f"{name} must be [B, H, N, d], got shape {a.shape}")
+    return a
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _mask(block_mask, N, mask_tile):
+    if block_mask is None:
+        return None
+    m = np.ascontiguousarray(np.asarray(block_mask, dtype=np.uint8))
+    T = (N + mask_tile - 1) // mask_tile
+    if m.shape != (T, T):
+        raise ValueError(f"block_mask must be [{T}, {T}] for N={N}, tile={mask_tile}")
+    return m
+
+
+def _idx(rows, N):
+    if rows is None:
+        return None
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    if r.ndim != 1 or (r.size and (r.min() < 0 or r.max() >= N)):
+        raise ValueError("row indices out of range")
+    return r
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with code {rc}")
+
+
+def forward(q, k, v, causal=False, scale=None, block_mask=None, mask_tile=128, rows=None,
+            threads=None):
+    """Exact attention from the definition: returns (O, LSE) in float64.
+
+    ``rows`` (optional) restricts the computation to those query rows; the
+    outputs are then ``[B, H, len(rows), d]`` and ``[B, H, len(rows)]``.
+    """
+    q, k, v = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one shape")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    m = _mask(block_mask, N, mask_tile)
+    r = _idx(rows, N)
+    nr = N if r is None else r.size
+    o = np.empty((B, H, nr, d), np.float64)
+    lse = np.empty((B, H, nr), np.float64)
+    if B * H * nr == 0:
+        return o, lse
+    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte), mask_tile,
+                                _ptr(r, ctypes.c_int), nr, threads or default_threads())
+    _check(rc, "oracle_forward")
+    return o, lse
+
+
+def forward_tiled(q, k, v, causal=False, scale=None, block_mask=None, mask_tile=128, bq=64,
+                  bk=64, threads=None):
+    """The online-softmax recurrence over bq x bk blocks: returns (O, LSE)."""
+    q, k, v = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one shape")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    m = _mask(block_mask, N, mask_tile)
+    o = np.empty((B, H, N, d), np.float64)
+    lse = np.empty((B, H, N), np.float64)
+    if B * H * N == 0:
+        return o, lse
+    rc = _load().oracle_forward_tiled(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
+                                      d, int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte),
+                                      mask_tile, int(bq), int(bk), threads or default_threads())
+    _check(rc, "oracle_forward_tiled")
+    return o, lse
+
+
+def backward(q, k, v, do, causal=False, scale=None, block_mask=None, mask_tile=128,
+             qrows=None, kcols=None, want_dq=True, want_dkv=True, threads=None):
+    """Analytic gradients of exact attention for upstream gradient ``do``.
+
+    Returns a dict with ``dq`` ([B,H,nq,d]), ``dk``/``dv`` ([B,H,nk,d]), and
+    ``lse``/``D`` ([B,H,N], the row statistics the oracle computed itself).
+    ``qrows``/``kcols`` restrict dq / dk,dv to those rows.
+    """
+    q, k, v, do = _f64(q, "q"), _f64(k, "k"), _f64(v, "v"), _f64(do, "do")
+    B, H, N, d = q.shape
+    if any(t.shape != q.shape for t in (k, v, do)):
+        raise ValueError("q, k, v, do must share one shape")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    m = _mask(block_mask, N, mask_tile)
+    # a non-NULL index array with count 0 tells the C side to skip that part
+    qr = _idx(qrows, N) if want_dq else np.zeros(1, np.int32)
+    kc = _idx(kcols, N) if want_dkv else np.zeros(1, np.int32)
+    nq = N if qr is None else (qr.size if want_dq else 0)
+    nk = N if kc is None else (kc.size if want_dkv else 0)
+    dq = np.empty((B, H, nq, d), np.float64)
+    dk = np.empty((B, H, nk, d), np.float64)
+    dv = np.empty((B, H, nk, d), np.float64)
+    lse = np.empty((B, H, N), np.float64)
+    D = np.empty((B, H, N), np.float64)
+    if B * H * N > 0:
+        rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(lse), _ptr(D), B, H, N, d,
+                                     int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte),
+                                     mask_tile, _ptr(qr, ctypes.c_int), nq,
+                                     _ptr(kc, ctypes.c_int), nk, threads or default_threads())
+        _check(rc, "oracle_backward")
+    return {"dq": dq, "dk": dk, "dv": dv, "lse": lse, "D": D}
