@@ -1,0 +1,431 @@
+// Fused attention forward for sm_103a: TMA loads, tcgen05 MMAs accumulating in
+// tensor memory, online softmax in registers.
+//
+// Method: the tiled forward pass with online softmax of "Paper Notes:
+// FlashAttention" (sections "Tiling: Block-by-Block Softmax" and "The Complete
+// Algorithm in Pseudocode"), in the corrected form of the numpy
+// flash_attention in "flash attention" (muhibwaqar.com, "build it from
+// scratch") and of the aicassindra page ("Rescale and accumulate: the forward
+// pass in one loop"): running max m and sum l per row, an unnormalised output
+// accumulator rescaled by exp(m_old - m_new), one division by l at the end.
+// Causal masking is applied per tile (aicassindra page, "Common pitfalls"):
+// tiles above the diagonal are never visited, diagonal tiles are masked
+// element-wise. Block-sparse attention ("Paper Notes: FlashAttention",
+// "Experiments & Results") visits only the tiles whose mask byte is set.
+//
+// CTA = one head, two consecutive 128-row Q tiles (t = 0, 1) sharing one
+// stream of K/V tiles. 12 warps:
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j through a smem ring
+//   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
+//   warp 2      builds the list of K/V tiles to visit, then idles
+//   warps 4-7   softmax of Q tile 0 (thread = query row = TMEM lane)
+//   warps 8-11  softmax of Q tile 1
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [0,128) S_0   [128,256) S_1   [256,256+d) O_0   [256+d,256+2d) O_1
+// The MMA issue order PV_0(n), S_0(n+1), PV_1(n), S_1(n+1) lets the tensor
+// core work on one Q tile while the other tile's softmax runs.
+#include <math.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kChunks = D / 64;              // 128-byte column chunks per row
+  static constexpr int kChunkBytes = kTile * 128;     // 128 rows x 128 B
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring slots (K and V alternate)
+  static constexpr int kPBytes = kTile * kTile * 2;   // bf16 P tile, 2 chunks of 64 keys
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + 2 * kTileBytes;
+  static constexpr int kPOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kListOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kListOff + kMaxTiles * 2;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, teardown
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+struct Bars {
+  uint32_t base;
+  int stages;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t kv_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t kv_empty(int s) const { return base + 8 * (1 + stages + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 2 * stages + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 2 * stages + t); }
+  __device__ uint32_t o_done() const { return base + 8 * (5 + 2 * stages); }
+  __device__ uint32_t teardown() const { return base + 8 * (6 + 2 * stages); }
+};
+
+// list entry: bits 0-11 key tile j, bit 14 visited by Q tile 0, bit 15 by Q tile 1
+__device__ __forceinline__ int entry_j(uint32_t e) { return int(e & 0xFFFu); }
+__device__ __forceinline__ bool entry_act(uint32_t e, int t) { return (e >> (14 + t)) & 1u; }
+
+enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + L::kQOff;
+  const uint32_t sKV = s_base + L::kKVOff;
+  const uint32_t sP = s_base + L::kPOff;
+  uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort
+  Bars bars{s_base + L::kBarOff, L::kStages};
+  StatusSlot st{p.status, &misc[2]};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // work item: heavy (late) Q-tile pairs first across all heads
+  const int T = p.n / kTile;
+  const int npairs = (T + 1) >> 1;
+  const int bh = blockIdx.x % p.bh;
+  const int pair = npairs - 1 - blockIdx.x / p.bh;
+  const int i0 = 2 * pair;
+  const bool has1 = (i0 + 1) < T;
+  const int qrow0 = bh * p.n + i0 * kTile;  // first global row of Q tile 0
+
+  // ---- setup -------------------------------------------------------------
+  if (warp == 0 && lane == 0) {
+    mbar_init(bars.q_full(), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bars.kv_full(s), 1);
+      mbar_init(bars.kv_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full(t), 1);
+      mbar_init(bars.p_full(t), 128);
+    }
+    mbar_init(bars.o_done(), 1);
+    mbar_init(bars.teardown(), 1);
+    misc[2] = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  } else if (warp == 1) {
+    tmem_alloc(smem_u32(&misc[0]), 512);
+    tmem_relinquish();
+  } else if (warp == 2) {
+    // K/V tiles visited by either Q tile, ascending, with per-tile flags
+    const int i1 = i0 + 1;
+    const int jmax = p.causal ? (has1 ? i1 : i0) : T - 1;
+    const uint8_t *m0 = p.mask ? p.mask + (size_t)i0 * T : nullptr;
+    const uint8_t *m1 = (p.mask && has1) ? p.mask + (size_t)i1 * T : nullptr;
+    int count = 0;
+    for (int base = 0; base <= jmax; base += 32) {
+      const int j = base + lane;
+      bool a0 = j <= jmax && (!p.causal || j <= i0) && (!m0 || m0[j] != 0);
+      bool a1 = has1 && j <= jmax && (!m1 || m1[j] != 0);
+      const uint32_t ball = __ballot_sync(0xffffffffu, a0 || a1);
+      if (a0 || a1) {
+        const int slot = count + __popc(ball & ((1u << lane) - 1u));
+        list[slot] = uint16_t(j | (a0 ? 1u << 14 : 0u) | (a1 ? 1u << 15 : 0u));
+      }
+      count += __popc(ball);
+    }
+    if (lane == 0) misc[1] = count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  const int count = misc[1];
+
+  if (warp == 0) {
+    // ---- TMA producer ------------------------------------------------------
+    if (elect_one()) {
+      int pos = 0;
+      bool ok = true;
+      const uint32_t qbytes = (has1 ? 2u : 1u) * L::kTileBytes;
+      if (count > 0) {
+        mbar_arrive_expect_tx(bars.q_full(), qbytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_2d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0, bars.q_full());
+        if (has1)
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_2d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0 + kTile,
+                        bars.q_full());
+      }
+      for (int n = 0; n < count && ok; ++n) {
+        const int kvrow = bh * p.n + entry_j(list[n]) * kTile;
+        for (int which = 0; which < 2 && ok; ++which, ++pos) {
+          const int s = pos % L::kStages;
+          const uint32_t u = pos / L::kStages;
+          ok = mbar_wait(bars.kv_empty(s), (u & 1u) ^ 1u, st, status_code(kKernFwd, kRoleLoad, 1));
+          if (!ok) break;
+          mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+          const CUtensorMap *tm = which ? &p.tm_v : &p.tm_k;
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_2d(sKV + s * L::kTileBytes + c * L::kChunkBytes, tm, c * 64, kvrow,
+                        bars.kv_full(s));
+        }
+      }
+      // teardown: wait (bounded) until every copy this thread issued has landed
+      if (count > 0) mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+      for (int s = 0; s < L::kStages && s < pos; ++s) {
+        const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
+        mbar_wait(bars.kv_full(s), (last / L::kStages) & 1u, st,
+                  status_code(kKernFwd, kRoleLoad, 3));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- tcgen05 issuer ----------------------------------------------------
+    if (elect_one()) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);  // Q K^T, both K-major
+      constexpr uint32_t kIdPV = idesc_bf16_f32(kTile, D, 0, 1);     // P V, V is MN-major
+      bool ok = count == 0 || mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
+      uint32_t pcount[2] = {0, 0};
+      bool first_pv[2] = {true, true};
+
+      auto issue_s = [&](int t, int kslot) {
+        const uint32_t q_base = sQ + t * L::kTileBytes;
+        const uint32_t k_base = sKV + kslot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + t * kTile, sdesc_sw128(q_base + off, 16, 1024),
+                      sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int vslot, bool first) {
+        const uint32_t p_base = sP + t * L::kPBytes;
+        const uint32_t v_base = sKV + vslot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 256 + t * D, sdesc_sw128(p_base + a_off, 16, 1024),
+                      sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
+                      (kk > 0 || !first) ? 1u : 0u);
+        }
+      };
+
+      if (ok && count > 0) {
+        // prologue: S for the first K tile
+        ok = mbar_wait(bars.kv_full(0), 0, st, status_code(kKernFwd, kRoleMma, 2));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t e = list[0];
+          for (int t = 0; t < 2; ++t)
+            if (entry_act(e, t)) {
+              issue_s(t, 0);
+              mma_commit(bars.s_full(t));
+            }
+          mma_commit(bars.kv_empty(0));
+        }
+      }
+      for (int n = 0; n < count && ok; ++n) {
+        const uint32_t e = list[n];
+        const int vpos = 2 * n + 1, kpos = 2 * n + 2;
+        const int vslot = vpos % L::kStages, kslot = kpos % L::kStages;
+        const bool has_next = n + 1 < count;
+        const uint32_t en = has_next ? list[n + 1] : 0u;
+        ok = mbar_wait(bars.kv_full(vslot), (vpos / L::kStages) & 1u, st,
+                       status_code(kKernFwd, kRoleMma, 3));
+        if (ok && has_next)
+          ok = mbar_wait(bars.kv_full(kslot), (kpos / L::kStages) & 1u, st,
+                         status_code(kKernFwd, kRoleMma, 4));
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (entry_act(e, t)) {
+            ok = mbar_wait(bars.p_full(t), pcount[t] & 1u, st,
+                           status_code(kKernFwd, kRoleMma, 5 + t));
+            if (!ok) break;
+            ++pcount[t];
+            tc_fence_after();
+            issue_pv(t, vslot, first_pv[t]);
+            first_pv[t] = false;
+          }
+          if (has_next && entry_act(en, t)) {
+            issue_s(t, kslot);
+            mma_commit(bars.s_full(t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bars.kv_empty(vslot));
+        if (has_next) mma_commit(bars.kv_empty(kslot));
+      }
+      if (ok && count > 0) mma_commit(bars.o_done());
+      // teardown: every MMA this thread issued has completed
+      mma_commit(bars.teardown());
+      mbar_wait(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- softmax -----------------------------------------------------------
+    const int t = (warp - 4) >> 2;                 // Q tile of this warpgroup
+    const int r = threadIdx.x - 128 * (1 + t);     // row within the tile = TMEM lane
+    const int qi = i0 + t;                         // Q tile index
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * kTile;
+    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const uint32_t p_row = sP + t * L::kPBytes + r * 128;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    uint32_t scount = 0;
+    bool ok = true, any = false;
+
+    if (t == 0 || has1) {
+      for (int n = 0; n < count; ++n) {
+        const uint32_t e = list[n];
+        if (!entry_act(e, t)) continue;
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.s_full(t), scount & 1u, st,
+                                               status_code(kKernFwd, kRoleSoftmax, 1 + t)));
+        if (!ok) break;
+        ++scount;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+        tmem_wait_ld();
+        float s[kTile];
+#pragma unroll
+        for (int x = 0; x < kTile; ++x) s[x] = __uint_as_float(sr[x >> 5][x & 31]);
+        if (p.causal && entry_j(e) == qi) {
+#pragma unroll
+          for (int x = 0; x < kTile; ++x)
+            if (x > r) s[x] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int x = 1; x < kTile; ++x) mx = fmaxf(mx, s[x]);
+        const float m_tile = mx * c;
+        const bool need = m_tile > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+          m_used = m_tile;
+        }
+        l *= alpha;
+        const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+        // P = exp2(s*c - m) -> bf16, written K-major with the 128-byte swizzle
+#pragma unroll
+        for (int u = 0; u < kTile / 8; ++u) {  // 16-byte unit u holds keys 8u..8u+7
+          uint32_t pk[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float p0 = ex2_approx(fmaf(s[8 * u + 2 * h], c, -m_sub));
+            const float p1 = ex2_approx(fmaf(s[8 * u + 2 * h + 1], c, -m_sub));
+            l += p0 + p1;
+            pk[h] = pack_bf16x2(p0, p1);
+          }
+          const uint32_t chunk = u >> 3, unit = u & 7;
+          st_shared_v4(p_row + chunk * L::kChunkBytes + ((unit ^ (r & 7)) << 4), pk[0], pk[1],
+                       pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        if (any && __any_sync(0xffffffffu, need)) {
+          // O *= alpha for this row. The PV MMA of the previous tile has
+          // completed: it was issued before this S tile, whose completion we
+          // waited for.
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t o[16];
+            tmem_ld16(tO + q * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            tmem_st16(tO + q * 16, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bars.p_full(t));
+        any = true;
+      }
+      // epilogue: O / l and LSE
+      if (ok && any)
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.o_done(), 0, st,
+                                               status_code(kKernFwd, kRoleSoftmax, 3)));
+      if (ok) {
+        tc_fence_after();
+        const size_t row = (size_t)(qrow0 + t * kTile + r);
+        const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          if (any) {
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = 0u;
+          }
+          if (p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row * D + q * 32);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(__uint_as_float(o[4 * x]) * inv_l,
+                                   __uint_as_float(o[4 * x + 1]) * inv_l,
+                                   __uint_as_float(o[4 * x + 2]) * inv_l,
+                                   __uint_as_float(o[4 * x + 3]) * inv_l);
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row * D + q * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l);
+              dst[x] = v;
+            }
+          }
+        }
+        // LSE = ln(sum_j exp(scale s_ij)) = ln2 * (m + log2 l)
+        p.lse[row] = (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  static bool configured = false;  // attribute set once per process (idempotent anyway)
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int T = p.n / kTile;
+  const int grid = ((T + 1) / 2) * p.bh;
+  fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream) {
+  if (p.d == 64) return launch_fwd_d<64>(p, stream);
+  if (p.d == 128) return launch_fwd_d<128>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

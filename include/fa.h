@@ -1,0 +1,118 @@
+/*
+ * fa.h: C ABI of the exact IO-aware attention library for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The library computes exact scaled dot-product attention
+ *
+ *     O = softmax(scale * Q K^T) V            per batch b and head h,
+ *
+ * as defined in "Paper Notes: FlashAttention" (bv003me.vercel.app), section
+ * "What Are We Computing?", with the 1/sqrt(d) score scale of the numpy
+ * attention_naive in "flash attention" (muhibwaqar.com), section "build it
+ * from scratch" (here an explicit argument). The forward pass is one fused
+ * tiled kernel with online softmax (same page, section "Tiling: Block-by-Block
+ * Softmax"; aicassindra page "FlashAttention", section "Rescale and
+ * accumulate") that writes only O and the per-row log-sum-exp; the backward
+ * pass recomputes the score tiles from Q, K and the log-sum-exp (aicassindra
+ * page, section "The backward pass: recompute instead of store").
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are contiguous row-major [B][H][N][d]; Q, K, V, O, dO, dQ, dK, dV
+ *    hold bf16 values (raw 16-bit storage, passed as void*); LSE is fp32
+ *    [B][H][N], the natural-log log-sum-exp of the scaled scores of each row.
+ *  - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
+ *    caller. The library never allocates, frees or synchronises; all work is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *    default stream). Inputs are only read.
+ *  - Supported: d in {64, 128}; N a positive multiple of 128; B, H >= 1;
+ *    B*H*N <= 2^31 - 1; scale finite and > 0. B*H*N == 0 is a no-op that
+ *    returns FA_OK.
+ *  - causal != 0: query i sees key j iff j <= i (0-based, equal lengths).
+ *  - block_mask: NULL for dense attention, else a DEVICE uint8 array
+ *    [T][T], T = N/128, shared by every (b, h); tile (i/128, j/128) is kept
+ *    iff its byte is non-zero. With causal also set, both must allow a key.
+ *    The pages name a block-sparse variant only ("Paper Notes:
+ *    FlashAttention", section "Experiments & Results"); this tile semantics
+ *    is this library's reading. A query row that sees no key gets O = 0 and
+ *    LSE = -inf.
+ *  - Host-detectable errors return at once, before anything is enqueued. A
+ *    failed launch returns FA_ERR_CUDA. Kernel-side bounded waits that give up
+ *    record FA_ERR_TIMEOUT in a device status word that fa_device_status()
+ *    reads.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale */
+  FA_ERR_UNSUPPORTED = 2, /* valid but outside the supported set (d, N) */
+  FA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 5      /* a kernel-side wait gave up (device status word) */
+} fa_status;
+
+/* Version of this ABI; bumped on any incompatible change. */
+int fa_abi_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fa_status_string(int status);
+
+/*
+ * Forward pass. Reads Q, K, V; writes O (bf16 [B,H,N,d]) and LSE
+ * (fp32 [B,H,N]). S and P never reach global memory.
+ */
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                     int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
+                     void *stream);
+
+/*
+ * Forward pass with an fp32 O store: the same kernel and arithmetic as
+ * fa_forward, but O is written as fp32 [B,H,N,d] before any bf16 rounding.
+ * It exists so that accuracy can be checked without the output rounding.
+ */
+fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, float *LSE,
+                         int B, int H, int N, int d, int causal, float scale,
+                         const uint8_t *block_mask, void *stream);
+
+/*
+ * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i)
+ * followed by an fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass. Reads Q, K, V, O, dO (bf16) and LSE (fp32, as written by the
+ * forward pass with the same arguments); writes dQ, dK, dV (bf16 [B,H,N,d]).
+ * `workspace` is a caller-owned device buffer of at least
+ * fa_backward_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents
+ * on entry do not matter and are clobbered. The score and probability tiles
+ * are recomputed on chip and never reach global memory.
+ */
+fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
+                      const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                      int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Debug/status query: synchronises `stream`, reads the device status word
+ * that kernel-side bounded waits set when they give up, clears it, and
+ * stores it in *code (0 = no failure; otherwise an encoded kernel/role/wait
+ * site). Returns FA_ERR_TIMEOUT if a wait gave up, FA_ERR_CUDA if the stream
+ * reports an error, else FA_OK.
+ */
+fa_status fa_device_status(void *stream, unsigned int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */
