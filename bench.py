@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = forward + backward of causal attention on the GPT-2-medium-shaped
+workload B=4, H=16, N=4096, d=128 (bf16 in, fp32 accumulation), inputs
+resident in HBM. FLOPs follow the method's count: 4 N^2 d per head for the
+forward, halved for causal, and 2.5x that for the backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
+
+Prints one JSON line on rank 0. With --gpus N > 1 (launched by torchrun) every
+rank runs the same per-GPU workload (independent heads, no collective on the
+data path): weak scaling, value = all ranks' FLOPs / the slowest rank's time.
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+WORKLOAD = "gpt2_medium_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (also exercised by CPU tests)
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def attention_flops(w, density: float = 1.0):
+    """(forward, backward) FLOPs of one pass over workload w."""
+    fwd = 4.0 * w.N * w.N * w.d * w.B * w.H * density * (0.5 if w.causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+class Dist:
+    """Host-side coordination of ranks (gloo): barrier and max/sum over ranks.
+    Used for timing only; the attention data never crosses ranks."""
+
+    def __init__(self):
+        self.rank, self.world, self.local_rank = dist_env()
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as td
+            if not td.is_initialized():
+                td.init_process_group("gloo")
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg and self.pg.is_initialized():
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.gpu, self.period = gpu_id, period_ms
+        self.proc, self.path = None, None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and parts[1].isdigit():
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    sm = [int(r[1]) for r in rows]
+    mx = max(int(r[2]) for r in rows)
+    power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+    busy = [s for s, r in zip(sm, rows) if float(r[3] or 0) > 300.0] or sm
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": reasons,
+            "samples": len(rows), "samples_under_load": len(busy),
+            "power_w_max": max(power) if power else None}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("fa_bwd.cu", "fa_fwd.cu", "ptx.cuh", "fa_internal.h"):
+        with open(os.path.join(ROOT, "exact_io_aware_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the summary is missing or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        entry = t["kernels"][kernel]
+        if t.get("source_hash") != kernel_source_hash():
+            return None
+        return float(entry["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+
+def oracle_sample_step(inp, w, head: int, rows_per_step: int):
+    """Oracle forward and backward for `rows_per_step` evenly spaced query rows
+    (and the same key rows) of one head. Returns (seconds, credited FLOPs):
+    the credit is the method's forward+backward FLOPs of those query rows."""
+    import numpy as np
+    import oracle
+    b, h = divmod(head % (w.B * w.H), w.H)
+    sl = lambda t: t[b:b + 1, h:h + 1].to("cpu").double().numpy()
+    q, k, v, do = (sl(inp[t]) for t in ("q", "k", "v", "do"))
+    stride = max(1, w.N // rows_per_step)
+    rows = (np.arange(rows_per_step) * stride + (head * 37) % stride).astype(np.int32)
+    rows = rows[rows < w.N]
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, causal=w.causal, scale=w.scale, rows=rows)
+    oracle.backward(q, k, v, do, causal=w.causal, scale=w.scale, qrows=rows, kcols=rows)
+    dt = time.perf_counter() - t0
+    visible = (rows + 1).sum() if w.causal else rows.size * w.N
+    return dt, 3.5 * 4.0 * w.d * float(visible)
+
+
+def oracle_baseline(w, inp, budget_s: float, rows_per_step: int = 256):
+    total_t = total_f = 0.0
+    steps = 0
+    while total_t < budget_s and steps < 256:
+        dt, fl = oracle_sample_step(inp, w, steps, rows_per_step)
+        total_t += dt
+        total_f += fl
+        steps += 1
+    import oracle
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"{steps} x ({rows_per_step} evenly spaced query rows and key rows of one "
+                      f"head of {WORKLOAD}, fp64 forward + backward); credited FLOPs = the "
+                      f"method's forward+backward FLOPs of those query rows",
+            "seconds": total_t}
+
+
+# ---------------------------------------------------------------------------
+# CUDA arm
+
+def run_cuda(args, dist: Dist):
+    import torch
+    import exact_io_aware_attention_gb300 as fa
+    from exact_io_aware_attention_gb300 import inputs as gen
+
+    w = gen.WORKLOADS[WORKLOAD]
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    host = gen.make_workload_inputs(w)            # seeded bf16 on the CPU
+    q, k, v, do = (host[t].to(dev) for t in ("q", "k", "v", "do"))
+    shape = (w.B, w.H, w.N, w.d)
+    o = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    ws = torch.empty(fa.backward_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws,
+                    dq=dq, dk=dk, dv=dv)
+
+    fwd_fl, bwd_fl = attention_flops(w)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel-side wait gave up during warm-up")
+
+    # ---- timed region: inputs resident in HBM ------------------------------
+    fa.profile_collect()
+    fa.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", dist.local_rank))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    with ClockSampler(gpu_id) as clocks:
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+    fa.profile_enable(False)
+    ms_total = e0.elapsed_time(e1)
+    per_kernel = fa.profile_collect()
+    clk = clocks.summary()
+    if fa.device_status() != 0:
+        raise RuntimeError("a kernel-side wait gave up in the timed region")
+
+    ms_max = dist.reduce(ms_total, "max")
+    flops_all = dist.reduce((fwd_fl + bwd_fl) * args.steps, "sum")
+    value = flops_all / (ms_max * 1e-3) / 1e12
+    ms_step = ms_max / args.steps
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    fwd_ms = per_kernel["fa_fwd_kernel"][0] / max(1, per_kernel["fa_fwd_kernel"][1])
+    bwd_parts = ["fa_bwd_pre", "fa_bwd_main", "fa_bwd_dq"]
+    bwd_ms = sum(per_kernel[k][0] for k in bwd_parts) / max(1, per_kernel["fa_bwd_main"][1])
+    main_ms, main_n = per_kernel["fa_bwd_main"]
+    main_avg = main_ms / max(1, main_n)
+    launches = sum(n for _, n in per_kernel.values())
+    dominant = max(per_kernel, key=lambda kname: per_kernel[kname][0])
+    dom_ms, dom_n = per_kernel[dominant]
+    dom_flops = {"fa_fwd_kernel": fwd_fl, "fa_bwd_main": bwd_fl}.get(dominant, 0.0)
+    achieved = dom_flops / (dom_ms / dom_n * 1e-3) / 1e12 if dom_n else 0.0
+
+    # ---- end to end through the public API with host buffers --------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {t: host[t].pin_memory() for t in ("q", "k", "v", "do")}
+        outs = {t: torch.empty(shape, dtype=torch.bfloat16).pin_memory() for t in ("dq", "dk", "dv")}
+
+        def e2e_step():
+            for t, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+                dst.copy_(pin[t], non_blocking=True)
+            step()
+            for t, src in (("dq", dq), ("dk", dk), ("dv", dv)):
+                outs[t].copy_(src, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        e0.record(stream)
+        n_e2e = max(1, args.steps // 2)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = dist.reduce(e0.elapsed_time(e1), "max")
+        e2e = {"value": dist.reduce((fwd_fl + bwd_fl) * n_e2e, "sum") / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "steps": n_e2e,
+               "h2d_bytes_per_step": sum(pin[t].numel() * 2 for t in pin),
+               "d2h_bytes_per_step": sum(outs[t].numel() * 2 for t in outs)}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(w, host, budget_s=15.0)
+
+    ws_bytes = 5 * q.numel() * 2 + ws.numel()
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) rounded to bf16)",
+        "config": {"workload": f"{WORKLOAD}: B={w.B} H={w.H} N={w.N} d={w.d} causal, "
+                               "forward + backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "scale": w.scale,
+                   "l2": f"inputs larger than L2 ({ws_bytes / 2**20:.0f} MiB touched per step "
+                         f"vs {L2_BYTES / 2**20:.0f} MiB L2)",
+                   "parallelism": f"replicas x{dist.world} (independent heads, no collective)"},
+        "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_fl / fwd_ms / 1e9, 1),
+                "frac_of_peak": round(fwd_fl / fwd_ms / 1e9 / peak, 4)},
+        "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_fl / bwd_ms / 1e9, 1),
+                "frac_of_peak": round(bwd_fl / bwd_ms / 1e9 / peak, 4),
+                "main_kernel_ms": round(main_avg, 4)},
+        "per_kernel_ms": {kname: round(t / n, 4) if n else None for kname, (t, n) in per_kernel.items()},
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                     "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS.json)"
+                                    if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                     "traffic": dram_traffic(dominant),
+                     "algorithmic_flops_per_launch": dom_flops},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    return result
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return None
+    from exact_io_aware_attention_gb300 import inputs as gen
+    import oracle
+
+    w = gen.WORKLOADS[WORKLOAD]
+    host = gen.make_workload_inputs(w)
+    # size each step so that the whole run stays within about three minutes
+    probe_t, _ = oracle_sample_step(host, w, 0, 64)
+    per_step_budget = 180.0 / (args.steps + args.warmup)
+    rows = int(max(8, min(w.N, 64 * per_step_budget / max(probe_t, 1e-3))))
+    for s in range(args.warmup):
+        oracle_sample_step(host, w, s, rows)
+    total_t = total_f = 0.0
+    for s in range(args.steps):
+        dt, fl = oracle_sample_step(host, w, args.warmup + s, rows)
+        total_t += dt
+        total_f += fl
+    value = total_f / total_t / 1e12
+    sample = (f"each step: oracle forward + backward for {rows} evenly spaced query rows and key "
+              f"rows of one head of {WORKLOAD}; credited FLOPs = the method's forward+backward "
+              "FLOPs of those query rows")
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1) rounded to bf16)", "impl": "reference",
+        "config": {"workload": f"{WORKLOAD}: B={w.B} H={w.H} N={w.N} d={w.d} causal, "
+                               "forward + backward (bounded row samples)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            result = run_reference(args, dist)
+        else:
+            result = run_cuda(args, dist)
+        if dist.rank == 0 and result is not None:
+            print(json.dumps(result), flush=True)
+    finally:
+        dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -27,11 +27,16 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "fa_abi_version": ([], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
+    "fa_last_error": ([], ctypes.c_char_p),
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_forward_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "fa_device_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i),
+    "fa_num_kernels": ([], _i),
+    "fa_kernel_name": ([_i], ctypes.c_char_p),
+    "fa_profile_enable": ([_i], _i),
+    "fa_profile_collect": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _i], _i),
 }
 
 _lock = threading.Lock()
@@ -39,9 +44,10 @@ _lib = None
 
 
 class FAError(RuntimeError):
-    def __init__(self, status: int, what: str):
+    def __init__(self, status: int, what: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        msg = f"{what}: {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 def load_library(path: str | None = None):
@@ -67,7 +73,8 @@ def load_library(path: str | None = None):
 
 def _check(status: int, what: str):
     if status != FA_OK:
-        raise FAError(status, what)
+        detail = load_library().fa_last_error().decode() if status == 4 else ""
+        raise FAError(status, what, detail)
 
 
 def _stream():
@@ -148,6 +155,22 @@ def device_status(stream=None) -> int:
     if rc not in (FA_OK, 5):
         raise FAError(rc, "fa_device_status")
     return int(code.value)
+
+
+def profile_enable(enable: bool = True):
+    """Bracket every kernel launch with CUDA events on its stream (no sync)."""
+    _check(load_library().fa_profile_enable(int(bool(enable))), "fa_profile_enable")
+
+
+def profile_collect() -> dict:
+    """{kernel name: (total ms, launches)} since the last collect; synchronises
+    on the recorded events."""
+    lib = load_library()
+    n = lib.fa_num_kernels()
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    _check(lib.fa_profile_collect(ms, cnt, n), "fa_profile_collect")
+    return {lib.fa_kernel_name(k).decode(): (float(ms[k]), int(cnt[k])) for k in range(n)}
 
 
 class _Attention(torch.autograd.Function):

@@ -4,9 +4,12 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -15,6 +18,15 @@ namespace {
 
 // Device status word written by kernel-side bounded waits that give up.
 __device__ unsigned int g_status_word = 0u;
+
+// Text of the last FA_ERR_CUDA failure of the calling thread.
+thread_local char g_last_error[256] = "";
+
+fa_status cuda_fail(const char *where, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+           (int)e);
+  return FA_ERR_CUDA;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -36,28 +48,52 @@ EncodeTiledFn encoder() {
   return g_encode;
 }
 
-unsigned int *status_word() {
-  // per device: the symbol address is looked up on the current device each call
+cudaError_t status_word(unsigned int **out) {
+  // looked up on the calling thread's current device at every call
   void *ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
-  return static_cast<unsigned int *>(ptr);
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_status_word);
+  *out = static_cast<unsigned int *>(ptr);
+  return e;
 }
 
 // 2-D bf16 map over [rows][d]: box = 64 columns (128 bytes) x 128 rows, 128-byte swizzle.
 bool encode_rows(CUtensorMap *m, const void *base, long long rows, int d) {
   EncodeTiledFn enc = encoder();
-  if (!enc) return false;
+  if (!enc) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)fa::kTile};
   const cuuint32_t elem[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  const CUresult r =
+      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    snprintf(g_last_error, sizeof(g_last_error),
+             "cuTensorMapEncodeTiled(base=%p, rows=%lld, d=%d) failed: CUresult %d", base, rows, d,
+             (int)r);
+  return r == CUDA_SUCCESS;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Makes the device that owns `ptr` current on the calling thread, which also
+// gives a thread that has not used CUDA yet (e.g. an autograd worker) a
+// current context for the driver calls that follow.
+fa_status bind_device(const void *ptr) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) return cuda_fail("cudaPointerGetAttributes", e);
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) {
+    snprintf(g_last_error, sizeof(g_last_error), "tensor at %p is not device memory", ptr);
+    return FA_ERR_INVALID_ARG;
+  }
+  e = cudaSetDevice(a.device);
+  return e == cudaSuccess ? FA_OK : cuda_fail("cudaSetDevice", e);
+}
 
 constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -86,6 +122,7 @@ fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, flo
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return FA_ERR_MISALIGNED;
+  if ((s = bind_device(Q)) != FA_OK) return s;
   fa::FwdParams p;
   memset(&p, 0, sizeof(p));
   const long long rows = (long long)B * H * N;
@@ -101,15 +138,100 @@ fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, flo
   p.causal = causal ? 1 : 0;
   p.o_f32 = o_f32;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  p.status = status_word();
-  if (!p.status) return FA_ERR_CUDA;
-  return fa::launch_forward(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
-                                                                                 : FA_ERR_CUDA;
+  cudaError_t e = status_word(&p.status);
+  if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+  e = fa::launch_forward(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
+}
+
+// ---- measurement hooks ------------------------------------------------------
+
+struct ProbeRecord {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+std::vector<ProbeRecord> g_prof_records;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
 }
 
 }  // namespace
 
+namespace fa {
+
+LaunchProbe::LaunchProbe(int kind, cudaStream_t stream) : slot_(-1), stream_(stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  ProbeRecord r{kind, pooled_event(), pooled_event()};
+  if (!r.start || !r.stop) return;
+  if (cudaEventRecord(r.start, stream) != cudaSuccess) return;
+  slot_ = (int)g_prof_records.size();
+  g_prof_records.push_back(r);
+}
+
+LaunchProbe::~LaunchProbe() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaEventRecord(g_prof_records[slot_].stop, stream_);
+}
+
+}  // namespace fa
+
 extern "C" {
+
+int fa_num_kernels(void) { return fa::kNumKinds; }
+
+const char *fa_kernel_name(int kind) {
+  switch (kind) {
+    case fa::kKindFwd: return "fa_fwd_kernel";
+    case fa::kKindBwdPre: return "fa_bwd_pre";
+    case fa::kKindBwdMain: return "fa_bwd_main";
+    case fa::kKindBwdDq: return "fa_bwd_dq";
+    default: return "";
+  }
+}
+
+fa_status fa_profile_enable(int enable) {
+  g_prof_on.store(enable != 0);
+  return FA_OK;
+}
+
+fa_status fa_profile_collect(float *total_ms, int *launches, int n) {
+  if ((!total_ms || !launches) && n > 0) return FA_ERR_INVALID_ARG;
+  for (int k = 0; k < n; ++k) {
+    total_ms[k] = 0.f;
+    launches[k] = 0;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  fa_status rc = FA_OK;
+  for (const ProbeRecord &r : g_prof_records) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) rc = cuda_fail("cudaEventElapsedTime", e);
+    if (r.kind >= 0 && r.kind < n) {
+      total_ms[r.kind] += ms;
+      launches[r.kind] += 1;
+    }
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_records.clear();
+  return rc;
+}
+
 
 int fa_abi_version(void) { return 1; }
 
@@ -140,7 +262,7 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
   const size_t rows = (size_t)B * H * N;
-  return round_up(rows * sizeof(float)) + round_up(rows * (size_t)d * sizeof(float));
+  return 2 * round_up(rows * sizeof(float)) + round_up(rows * (size_t)d * sizeof(float));
 }
 
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
@@ -157,6 +279,7 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
       !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) ||
       (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
     return FA_ERR_MISALIGNED;
+  if ((s = bind_device(Q)) != FA_OK) return s;
   fa::BwdParams p;
   memset(&p, 0, sizeof(p));
   const long long rows = (long long)B * H * N;
@@ -166,9 +289,10 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
   p.o = O;
   p.dout = dO;
   p.lse = LSE;
+  const size_t stat_bytes = round_up((size_t)rows * sizeof(float));
   p.delta = static_cast<float *>(workspace);
-  p.dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                       round_up((size_t)rows * sizeof(float)));
+  p.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + stat_bytes);
+  p.dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * stat_bytes);
   p.dq = dQ;
   p.dk = dK;
   p.dv = dV;
@@ -179,23 +303,27 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.status = status_word();
-  if (!p.status) return FA_ERR_CUDA;
-  return fa::launch_backward(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
-                                                                                  : FA_ERR_CUDA;
+  cudaError_t e = status_word(&p.status);
+  if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+  e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
 }
 
 fa_status fa_device_status(void *stream, unsigned int *code) {
   if (!code) return FA_ERR_INVALID_ARG;
   *code = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
   unsigned int w = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w)) != cudaSuccess) return FA_ERR_CUDA;
-  if (w && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
-    return FA_ERR_CUDA;
+  e = cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w));
+  if (e != cudaSuccess) return cuda_fail("cudaMemcpyFromSymbol", e);
+  if (w && (e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess)
+    return cuda_fail("cudaMemcpyToSymbol", e);
   *code = w;
   return w ? FA_ERR_TIMEOUT : FA_OK;
 }
+
+const char *fa_last_error(void) { return g_last_error; }
 
 }  // extern "C"

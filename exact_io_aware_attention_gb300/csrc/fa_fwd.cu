@@ -416,7 +416,10 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   }
   const int T = p.n / kTile;
   const int grid = ((T + 1) / 2) * p.bh;
-  fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(p);
+  {
+    LaunchProbe probe(kKindFwd, stream);
+    fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

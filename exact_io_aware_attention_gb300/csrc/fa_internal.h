@@ -27,12 +27,28 @@ struct BwdParams {
   const void *o, *dout;               // bf16 [B*H*N][d]
   const float *lse;                   // [B*H*N]
   float *delta;                       // workspace: D_i [B*H*N]
+  float *lse2;                        // workspace: LSE_i * log2(e) [B*H*N]
   float *dq_acc;                      // workspace: fp32 [B*H*N][d]
   void *dq, *dk, *dv;                 // bf16 outputs
   const uint8_t *mask;
   int bh, n, d, causal;
   float scale, scale_log2;
   unsigned int *status;
+};
+
+// Kernel ids of the measurement hooks (names in fa_kernel_name()).
+enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdDq = 3,
+                        kNumKinds = 4 };
+
+// Brackets one launch with CUDA events when measurement is enabled
+// (fa_profile_enable); a no-op otherwise.
+class LaunchProbe {
+ public:
+  LaunchProbe(int kind, cudaStream_t stream);
+  ~LaunchProbe();
+ private:
+  int slot_;
+  cudaStream_t stream_;
 };
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);

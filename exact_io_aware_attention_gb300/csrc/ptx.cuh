@@ -83,7 +83,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase of parity `parity` of barrier `bar` to complete.
 // Returns false (and records `code`) if it gives up or if another role of
 // this CTA already gave up.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, StatusSlot st,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, StatusSlot st,
                                             uint32_t code) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
@@ -118,6 +118,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -23,7 +23,8 @@
  *  - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
  *    caller. The library never allocates, frees or synchronises; all work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
- *    default stream). Inputs are only read.
+ *    default stream), which must belong to the device that holds Q. Each call
+ *    makes that device current on the calling thread. Inputs are only read.
  *  - Supported: d in {64, 128}; N a positive multiple of 128; B, H >= 1;
  *    B*H*N <= 2^31 - 1; scale finite and > 0. B*H*N == 0 is a no-op that
  *    returns FA_OK.
@@ -52,7 +53,7 @@ extern "C" {
 
 typedef enum fa_status {
   FA_OK = 0,
-  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale */
+  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, host memory */
   FA_ERR_UNSUPPORTED = 2, /* valid but outside the supported set (d, N) */
   FA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
@@ -64,6 +65,13 @@ int fa_abi_version(void);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fa_status_string(int status);
+
+/*
+ * Description of the last FA_ERR_CUDA returned to the calling thread: the
+ * failing CUDA call and its error text ("" if none). Thread-local storage,
+ * valid until the thread's next failing call; never NULL.
+ */
+const char *fa_last_error(void);
 
 /*
  * Forward pass. Reads Q, K, V; writes O (bf16 [B,H,N,d]) and LSE
@@ -83,9 +91,9 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
                          const uint8_t *block_mask, void *stream);
 
 /*
- * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i)
- * followed by an fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i),
+ * fp32 LSE*log2(e) [B,H,N] and an fp32 dQ accumulator [B,H,N,d], each
+ * starting on a 256-byte boundary. Returns 0 for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
@@ -110,6 +118,26 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
  * reports an error, else FA_OK.
  */
 fa_status fa_device_status(void *stream, unsigned int *code);
+
+/*
+ * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
+ * 0 forward, 1 backward preprocess (D_i, LSE*log2 e, zeroed dQ accumulator),
+ * 2 backward main, 3 backward dQ conversion; fa_kernel_name() names them
+ * ("" for an unknown id).
+ *
+ * fa_profile_enable(1): from then on every kernel launch is bracketed by two
+ * CUDA events recorded on its stream (no synchronisation, no device memory).
+ * fa_profile_enable(0) stops recording. Thread-safe.
+ *
+ * fa_profile_collect: waits for the recorded events, writes the summed
+ * event-timed duration (ms) and the launch count of kernel k into
+ * total_ms[k] and launches[k] for k < n, and forgets the records. Returns
+ * FA_ERR_CUDA if an event could not be read (fa_last_error() says which).
+ */
+int fa_num_kernels(void);
+const char *fa_kernel_name(int kernel);
+fa_status fa_profile_enable(int enable);
+fa_status fa_profile_collect(float *total_ms, int *launches, int n);
 
 #ifdef __cplusplus
 }

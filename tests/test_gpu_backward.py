@@ -1,0 +1,156 @@
+"""Parity of the CUDA backward pass (through the C ABI) with the fp64 oracle's
+analytic gradients. Small shapes: every element. Full-size workloads: dQ on
+sampled query rows and dK/dV on sampled key rows, which the oracle computes
+one by one from its own row statistics."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_attention_gb300 import inputs as gen
+from parity import check_grad, f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def fa():
+    import exact_io_aware_attention_gb300 as m
+    return m
+
+
+def run_fwd_bwd(inp, causal, scale, mask):
+    q, k, v, do = (inp[t].cuda() for t in ("q", "k", "v", "do"))
+    m = mask.cuda() if mask is not None else None
+    o, lse = fa().forward(q, k, v, causal=causal, scale=scale, block_mask=m)
+    dq, dk, dv = fa().backward(q, k, v, o, do, lse, causal=causal, scale=scale, block_mask=m)
+    torch.cuda.synchronize()
+    assert fa().device_status() == 0
+    return dq, dk, dv
+
+
+def full_check(B, H, N, d, causal, case, mask=None, scale=None, what=""):
+    inp = gen.make_inputs(B, H, N, d, case)
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    g = oracle.backward(*(f64(inp[t]) for t in ("q", "k", "v", "do")), causal=causal,
+                        scale=scale, block_mask=None if mask is None else mask.numpy())
+    dq, dk, dv = run_fwd_bwd(inp, causal, scale, mask)
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        check_grad(f64(x), g[name], name, what)
+    return g, (f64(dq), f64(dk), f64(dv))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [128, 256, 384, 640])
+def test_backward_small_shapes(N, d, causal):
+    full_check(1, 2, N, d, causal, case=400 + N + d, what=f"N={N} d={d} causal={causal}")
+
+
+def test_backward_single_head_n256_d64():
+    w = gen.WORKLOADS["single_head_n256_d64"]
+    full_check(w.B, w.H, w.N, w.d, w.causal, case=w.case, what=w.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_block_sparse_small(causal, d):
+    N = 1024
+    T = N // 128
+    mask = gen.block_mask(T, 0.25, seed=888 + d)
+    mask[3, :] = 0   # queries 384..511 see nothing: dQ = 0
+    mask[:, 6] = 0   # keys 768..895 are seen by nobody: dK = dV = 0
+    g, (dq, dk, dv) = full_check(2, 2, N, d, causal, case=500 + d, mask=mask,
+                                 what=f"sparse d={d} causal={causal}")
+    assert (dq[:, :, 384:512] == 0).all()
+    assert (dk[:, :, 768:896] == 0).all() and (dv[:, :, 768:896] == 0).all()
+
+
+def test_backward_peaked_softmax():
+    """Score std ~16 (q, k doubled, scale 0.5): rows are nearly one-hot. D_i is
+    formed from the stored bf16 O (D_i = dO_i . O_i), and its rounding error
+    (~2^-9 |dO_i||O_i| / sqrt(3)) does not shrink while dP_ij - D_i for the
+    dominant key does, so dS loses relative accuracy there. dV does not use D
+    and keeps the standard tolerance; dQ and dK are held to 2e-2."""
+    inp = gen.make_inputs(1, 2, 512, 64, case=600)
+    for t in ("q", "k"):
+        inp[t] = (inp[t].float() * 2).to(torch.bfloat16)
+    g = oracle.backward(*(f64(inp[t]) for t in ("q", "k", "v", "do")), scale=0.5)
+    dq, dk, dv = run_fwd_bwd(inp, False, 0.5, None)
+    check_grad(f64(dv), g["dv"], "dv", "peaked")
+    for name, x in (("dq", dq), ("dk", dk)):
+        r = rel_l2(f64(x), g[name])
+        assert r <= 2e-2, f"peaked {name} rel_l2={r:.3e}"
+
+
+def test_backward_repeatable_within_tolerance():
+    """dQ is accumulated with fp32 atomics (order varies); dK and dV are not."""
+    inp = gen.make_inputs(2, 2, 1024, 128, case=601)
+    a = run_fwd_bwd(inp, True, None, None)
+    b = run_fwd_bwd(inp, True, None, None)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+
+
+def test_autograd_wrapper_matches_backward():
+    inp = gen.make_inputs(1, 2, 256, 64, case=602)
+    q, k, v, do = (inp[t].cuda() for t in ("q", "k", "v", "do"))
+    qg, kg, vg = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = fa().attention(qg, kg, vg, causal=True)
+    out.backward(do)
+    dq, dk, dv = run_fwd_bwd(inp, True, None, None)
+    assert torch.equal(qg.grad, dq) or (qg.grad.float() - dq.float()).abs().max() < 1e-2
+    assert torch.equal(kg.grad, dk) and torch.equal(vg.grad, dv)
+
+
+EDGE_ROWS = (0, 1, 2, 127, 128, 129)
+
+
+@pytest.mark.parametrize("name", ["gpt2_small_causal", "gpt2_medium_causal", "gpt2_medium_dense",
+                                  "block_sparse_n8192"])
+def test_backward_full_size_whole_heads(name):
+    """Full-size workloads in the benchmark's launch configuration; the oracle
+    computes every gradient row of two heads, so the rel-L2 gate is evaluated
+    exactly on those heads."""
+    w = gen.WORKLOADS[name]
+    inp = gen.make_workload_inputs(w)
+    mask = inp["mask"]
+    dq, dk, dv = run_fwd_bwd(inp, w.causal, w.scale, mask)
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        g = oracle.backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["do"]),
+                            causal=w.causal, scale=w.scale,
+                            block_mask=None if mask is None else mask.numpy())
+        what = f"{name} b={b} h={h}"
+        check_grad(f64(dq[b, h]), g["dq"][0, 0], "dq", what)
+        check_grad(f64(dk[b, h]), g["dk"][0, 0], "dk", what)
+        check_grad(f64(dv[b, h]), g["dv"][0, 0], "dv", what)
+
+
+def test_backward_long_context_sampled_rows():
+    """B=1, H=16, N=65536, d=128, causal. The oracle's cost per head is ~1e12
+    flops, so rel-L2 is estimated on uniformly drawn query rows (dQ) and key
+    rows (dK, dV) of one head; the first rows of each tile boundary are
+    checked for gross errors (a wrong mask or a missing tile gives O(1)
+    errors; near one-hot rows carry the D_i rounding effect, see
+    test_backward_peaked_softmax)."""
+    w = gen.WORKLOADS["long_context_n65536"]
+    inp = gen.make_workload_inputs(w)
+    dq, dk, dv = run_fwd_bwd(inp, w.causal, w.scale, None)
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    rng = np.random.default_rng(w.case + 7)
+    rows = np.sort(rng.choice(w.N, 48, replace=False)).astype(np.int32)
+    keys = np.sort(rng.choice(w.N, 48, replace=False)).astype(np.int32)
+    edge = np.array(EDGE_ROWS + (w.N - 1,), np.int32)
+    sl = lambda t: f64(t[0:1, 0:1])
+    g = oracle.backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["do"]), causal=True,
+                        scale=w.scale, qrows=np.concatenate([rows, edge]),
+                        kcols=np.concatenate([keys, edge]))
+    n = rows.size
+    check_grad(f64(dq[0, 0, rows]), g["dq"][0, 0, :n], "dq", "long sampled")
+    check_grad(f64(dk[0, 0, keys]), g["dk"][0, 0, :n], "dk", "long sampled")
+    check_grad(f64(dv[0, 0, keys]), g["dv"][0, 0, :n], "dv", "long sampled")
+    for name, x, idx in (("dq", dq, edge), ("dk", dk, edge), ("dv", dv, edge)):
+        ref = g[name][0, 0, n:]
+        err = np.abs(f64(x[0, 0, idx]) - ref).max()
+        assert err <= 5e-2 * max(1e-3, np.abs(ref).max()), f"long edge rows {name} err={err:.3e}"
