@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_forward_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "fa_backward_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp], _i),
+    "fa_backward_noalloc_max_bytes": ([], _sz),
     "fa_device_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i),
     "fa_num_kernels": ([], _i),
     "fa_kernel_name": ([_i], ctypes.c_char_p),

@@ -167,6 +167,37 @@ cudaEvent_t pooled_event() {
   return e;
 }
 
+// ---- fixed scratch for fa_backward_noalloc ----------------------------------
+
+// The backward workspace of fa_backward_noalloc: a fixed area in the module's
+// global memory, so that call needs no allocation. Every device that loads
+// the library reserves it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device `dev`, looked up
+// once per device. (In host code the symbol's name is only a host-side
+// handle; its device address has to be asked for.)
+fa_status noalloc_scratch(int dev, void **out) {
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(g_last_error, sizeof(g_last_error), "device ordinal %d out of range", dev);
+    return FA_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress(noalloc scratch)", e);
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return FA_OK;
+}
+
 }  // namespace
 
 namespace fa {
@@ -325,5 +356,33 @@ fa_status fa_device_status(void *stream, unsigned int *code) {
 }
 
 const char *fa_last_error(void) { return g_last_error; }
+
+size_t fa_backward_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const void *O,
+                              const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const uint8_t *block_mask, void *stream) {
+  bool empty;
+  fa_status s = check_shape(B, H, N, d, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_backward_workspace_bytes(B, H, N, d);
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "fa_backward_noalloc: B=%d H=%d N=%d d=%d needs %zu bytes of scratch; the fixed "
+             "area holds %zu",
+             B, H, N, d, need, kNoAllocScratchBytes);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if ((s = bind_device(Q)) != FA_OK) return s;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  void *scratch = nullptr;
+  if ((s = noalloc_scratch(dev, &scratch)) != FA_OK) return s;
+  return fa_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, block_mask,
+                     scratch, need, stream);
+}
 
 }  // extern "C"

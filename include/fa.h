@@ -67,9 +67,11 @@ int fa_abi_version(void);
 const char *fa_status_string(int status);
 
 /*
- * Description of the last FA_ERR_CUDA returned to the calling thread: the
- * failing CUDA call and its error text ("" if none). Thread-local storage,
- * valid until the thread's next failing call; never NULL.
+ * Description of the last failure reported to the calling thread: for
+ * FA_ERR_CUDA the failing CUDA call and its error text, for a size that
+ * fa_backward_noalloc cannot hold the bytes needed and available ("" if
+ * none). Thread-local storage, valid until the thread's next failing call;
+ * never NULL.
  */
 const char *fa_last_error(void);
 
@@ -109,6 +111,38 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
                       int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass without a caller-supplied workspace. The pages have no
+ * counterpart: this entry point exists for callers of this library that
+ * cannot allocate device memory where they run the backward pass, e.g. a
+ * plug-in inside a host application that owns all device memory and gives
+ * plug-ins no allocator, or a runtime whose rules forbid allocating once it
+ * has started. Such a caller cannot provide fa_backward's workspace, so this
+ * call uses a scratch area of fixed size built into the library instead.
+ *
+ * Arguments, layouts, results and errors are those of fa_backward, minus
+ * the workspace. The scratch is a global-memory area of
+ * fa_backward_noalloc_max_bytes() bytes (64 MiB) that every device which
+ * loads the library reserves until the process exits. A call whose
+ * fa_backward_workspace_bytes(B,H,N,d) exceeds it returns FA_ERR_UNSUPPORTED
+ * before doing anything, and fa_last_error() states both sizes. The call
+ * allocates no memory (no cudaMalloc, no cudaFree, no allocating library
+ * routine) as long as the measurement hooks are off, which is the default.
+ *
+ * The first call on a device looks up the scratch area's device address on
+ * that device; make that first call before any stream capture. All calls on
+ * a device share the one area, and it keeps the last call's contents (each
+ * call re-initialises what must start at zero itself). Calls that overlap
+ * on the GPU, e.g. on two streams at once, race on the area: serialise them.
+ */
+fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const void *O,
+                              const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const uint8_t *block_mask, void *stream);
+
+/* Size in bytes of fa_backward_noalloc's fixed scratch area. */
+size_t fa_backward_noalloc_max_bytes(void);
 
 /*
  * Debug/status query: synchronises `stream`, reads the device status word
