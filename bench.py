@@ -46,6 +46,10 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (profiling runs; the benchmark uses the default)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (profiling runs only)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -233,12 +237,21 @@ def oracle_baseline(w, inp, budget_s: float, rows_per_step: int = 256):
 # ---------------------------------------------------------------------------
 # CUDA arm
 
+def select_workload(args):
+    import dataclasses
+    from exact_io_aware_attention_gb300 import inputs as gen
+    w = gen.WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = dataclasses.replace(w, B=args.batch)
+    return w
+
+
 def run_cuda(args, dist: Dist):
     import torch
     import exact_io_aware_attention_gb300 as fa
     from exact_io_aware_attention_gb300 import inputs as gen
 
-    w = gen.WORKLOADS[WORKLOAD]
+    w = select_workload(args)
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     host = gen.make_workload_inputs(w)            # seeded bf16 on the CPU
@@ -249,13 +262,15 @@ def run_cuda(args, dist: Dist):
     dq, dk, dv = (torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
     ws = torch.empty(fa.backward_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    mask = host["mask"].to(dev) if host["mask"] is not None else None
+    density = float(host["mask"].float().mean()) if host["mask"] is not None else 1.0
 
     def step():
-        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
-        fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws,
-                    dq=dq, dk=dk, dv=dv)
+        fa.forward(q, k, v, causal=w.causal, scale=w.scale, block_mask=mask, out=o, lse=lse)
+        fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, block_mask=mask,
+                    workspace=ws, dq=dq, dk=dk, dv=dv)
 
-    fwd_fl, bwd_fl = attention_flops(w)
+    fwd_fl, bwd_fl = attention_flops(w, density)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -343,8 +358,10 @@ def run_cuda(args, dist: Dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded iid N(0,1) rounded to bf16)",
-        "config": {"workload": f"{WORKLOAD}: B={w.B} H={w.H} N={w.N} d={w.d} causal, "
-                               "forward + backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} "
+                               f"{'causal' if w.causal else 'non-causal'}"
+                               f"{'' if w.sparse_density is None else f', block-sparse (kept {density:.4f})'}"
+                               ", forward + backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "scale": w.scale,
                    "l2": f"inputs larger than L2 ({ws_bytes / 2**20:.0f} MiB touched per step "
                          f"vs {L2_BYTES / 2**20:.0f} MiB L2)",
