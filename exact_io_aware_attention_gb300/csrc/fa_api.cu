@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -76,6 +77,16 @@ bool encode_rows(CUtensorMap *m, const void *base, long long rows, int d) {
              "cuTensorMapEncodeTiled(base=%p, rows=%lld, d=%d) failed: CUresult %d", base, rows, d,
              (int)r);
   return r == CUDA_SUCCESS;
+}
+
+// Heads per CTA group of the backward grid (kept small so the fp32 dQ rows
+// that concurrent CTAs accumulate stay in L2). FA_BWD_HEAD_GROUP overrides it
+// for tuning runs.
+int backward_head_group(int bh) {
+  const char *e = getenv("FA_BWD_HEAD_GROUP");
+  const int from_env = e ? atoi(e) : 0;
+  const int g = from_env > 0 ? from_env : 8;
+  return g < bh ? g : bh;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -334,6 +345,7 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.head_group = backward_head_group(p.bh);
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
   e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));

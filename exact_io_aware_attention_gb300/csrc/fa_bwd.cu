@@ -115,9 +115,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int T = p.n / kTile;
-  // heavy K/V tiles first: with causal masking tile j sees T - j Q tiles
-  const int bh = blockIdx.x % p.bh;
-  const int j = blockIdx.x / p.bh;
+  // CTAs are ordered head group by head group (p.head_group heads at a time),
+  // so that the fp32 dQ rows being accumulated by concurrent CTAs stay in L2;
+  // within a group the heavy K/V tiles come first (causal: tile j sees T - j
+  // Q tiles).
+  const int hg = p.head_group;
+  const int group = blockIdx.x / (hg * T);
+  const int g_base = group * hg;
+  const int g_size = min(hg, p.bh - g_base);
+  const int g_rank = blockIdx.x - group * hg * T;
+  const int j = g_rank / g_size;
+  const int bh = g_base + g_rank % g_size;
   const int first = next_q(p, p.causal ? j : 0, j, T);
   const bool any = first < T;
   const size_t kvrow = (size_t)bh * p.n + (size_t)j * kTile;
@@ -305,22 +313,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
       tc_fence_after();
       const float *lse2 = stat + s * 2 * kTile;
       const float *delta = lse2 + kTile;
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + L::kColS + q * 32, sr[q]);
-      tmem_wait_ld();
-      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); hidden entries 0
+      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); hidden entries 0.
+      // S^T is read 32 columns at a time to keep register pressure low.
       const bool diag = p.causal && i == j;
       uint32_t pk[64];
 #pragma unroll
-      for (int x = 0; x < kTile; x += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[x >> 5][x & 31]), c, -lse2[x]));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[(x + 1) >> 5][(x + 1) & 31]), c, -lse2[x + 1]));
-        if (diag) {
-          if (x < kr) p0 = 0.f;
-          if (x + 1 < kr) p1 = 0.f;
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sr[32];
+        tmem_ld32(tmem + lane_off + L::kColS + q * 32, sr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const int col = 32 * q + x;
+          const float2 l2 = *reinterpret_cast<const float2 *>(lse2 + col);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), c, -l2.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), c, -l2.y));
+          if (diag) {
+            if (col < kr) p0 = 0.f;
+            if (col + 1 < kr) p1 = 0.f;
+          }
+          pk[col >> 1] = pack_bf16x2(p0, p1);
         }
-        pk[x >> 1] = pack_bf16x2(p0, p1);
       }
       // the shared P^T/dS^T tile is free once the previous dK/dQ MMAs are done
       if (n > 0) {

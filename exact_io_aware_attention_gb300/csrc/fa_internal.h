@@ -32,6 +32,7 @@ struct BwdParams {
   void *dq, *dk, *dv;                 // bf16 outputs
   const uint8_t *mask;
   int bh, n, d, causal;
+  int head_group;                     // CTA order: heads per group (1..bh)
   float scale, scale_log2;
   unsigned int *status;
 };
