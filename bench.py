@@ -173,7 +173,7 @@ def summarize_clocks(rows):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("fa_bwd.cu", "fa_fwd.cu", "ptx.cuh", "fa_internal.h"):
+    for f in ("fa_bwd.cu", "fa_bwd_dq.cu", "fa_fwd.cu", "ptx.cuh", "fa_internal.h"):
         with open(os.path.join(ROOT, "exact_io_aware_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -309,14 +309,17 @@ def run_cuda(args, dist: Dist):
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
     fwd_ms = per_kernel["fa_fwd_kernel"][0] / max(1, per_kernel["fa_fwd_kernel"][1])
-    bwd_parts = ["fa_bwd_pre", "fa_bwd_main", "fa_bwd_dq"]
-    bwd_ms = sum(per_kernel[k][0] for k in bwd_parts) / max(1, per_kernel["fa_bwd_main"][1])
-    main_ms, main_n = per_kernel["fa_bwd_main"]
-    main_avg = main_ms / max(1, main_n)
+    bwd_parts = ["fa_bwd_pre", "fa_bwd_dkdv", "fa_bwd_dq"]
+    bwd_ms = sum(per_kernel[k][0] for k in bwd_parts) / max(1, per_kernel["fa_bwd_dkdv"][1])
+    avg = lambda kname: per_kernel[kname][0] / max(1, per_kernel[kname][1])
     launches = sum(n for _, n in per_kernel.values())
     dominant = max(per_kernel, key=lambda kname: per_kernel[kname][0])
     dom_ms, dom_n = per_kernel[dominant]
-    dom_flops = {"fa_fwd_kernel": fwd_fl, "fa_bwd_main": bwd_fl}.get(dominant, 0.0)
+    # the method's GEMMs each kernel performs: the forward's two; dK/dV runs four
+    # of the backward's five (S^T, dP^T, dV, dK); the dQ kernel runs the fifth
+    # (dQ) and recomputes S and dP, which is not credited
+    alg_flops = {"fa_fwd_kernel": fwd_fl, "fa_bwd_dkdv": 0.8 * bwd_fl, "fa_bwd_dq": 0.2 * bwd_fl}
+    dom_flops = alg_flops.get(dominant, 0.0)
     achieved = dom_flops / (dom_ms / dom_n * 1e-3) / 1e12 if dom_n else 0.0
 
     # ---- end to end through the public API with host buffers --------------
@@ -370,7 +373,10 @@ def run_cuda(args, dist: Dist):
                 "frac_of_peak": round(fwd_fl / fwd_ms / 1e9 / peak, 4)},
         "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_fl / bwd_ms / 1e9, 1),
                 "frac_of_peak": round(bwd_fl / bwd_ms / 1e9 / peak, 4),
-                "main_kernel_ms": round(main_avg, 4)},
+                "dkdv_kernel_ms": round(avg("fa_bwd_dkdv"), 4),
+                "dq_kernel_ms": round(avg("fa_bwd_dq"), 4),
+                "dq_kernel_executed_tflops": round(0.6 * bwd_fl / avg("fa_bwd_dq") / 1e9, 1)
+                if per_kernel["fa_bwd_dq"][1] else None},
         "per_kernel_ms": {kname: round(t / n, 4) if n else None for kname, (t, n) in per_kernel.items()},
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),

@@ -239,7 +239,7 @@ const char *fa_kernel_name(int kind) {
   switch (kind) {
     case fa::kKindFwd: return "fa_fwd_kernel";
     case fa::kKindBwdPre: return "fa_bwd_pre";
-    case fa::kKindBwdMain: return "fa_bwd_main";
+    case fa::kKindBwdDkdv: return "fa_bwd_dkdv";
     case fa::kKindBwdDq: return "fa_bwd_dq";
     default: return "";
   }
@@ -304,7 +304,7 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
   const size_t rows = (size_t)B * H * N;
-  return 2 * round_up(rows * sizeof(float)) + round_up(rows * (size_t)d * sizeof(float));
+  return 2 * round_up(rows * sizeof(float));
 }
 
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
@@ -334,7 +334,6 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
   const size_t stat_bytes = round_up((size_t)rows * sizeof(float));
   p.delta = static_cast<float *>(workspace);
   p.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + stat_bytes);
-  p.dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * stat_bytes);
   p.dq = dQ;
   p.dk = dK;
   p.dv = dV;

@@ -1,4 +1,4 @@
-// Attention backward for sm_103a, by recomputation.
+// Attention backward for sm_103a, by recomputation: preprocess and dK/dV.
 //
 // The pages store only O and the softmax statistics and regenerate S and P
 // block by block in the backward pass ("Paper Notes: FlashAttention",
@@ -14,22 +14,26 @@
 //   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
 //
 // Three kernels on the caller's stream:
-//   fa_bwd_pre   D_i, LSE_i * log2(e), and a zeroed fp32 dQ accumulator
-//   fa_bwd_main  one CTA per 128-key K/V tile; loops over the Q tiles that
-//                see it (causal: i >= j; block-sparse: mask[i][j] != 0)
-//   fa_bwd_dq    dQ = bf16(scale * dQ accumulator)
+//   fa_bwd_pre        D_i and LSE_i * log2(e)
+//   fa_bwd_dkdv       one CTA per 128-key K/V tile, looping over the Q tiles
+//                     that see it (causal: i >= j; block-sparse: mask[i][j]);
+//                     dK and dV accumulate in tensor memory (this file)
+//   fa_bwd_dq_kernel  one CTA per Q tile, looping over its K/V tiles; dQ
+//                     accumulates in tensor memory (fa_bwd_dq.cu)
+// Each gradient is owned by one CTA, so no cross-CTA reduction is needed;
+// the price is that S and dP are recomputed by both kernels.
 //
-// fa_bwd_main, 12 warps:
+// fa_bwd_dkdv, 12 warps:
 //   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per step (2 stages)
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
-//   warps 4-7   thread = key row: P^T from S^T, dS^T from dP^T, then dV out
-//   warps 8-11  dQ partial of each step -> fp32 reductions into global; then dK out
+//   warps 4-7   thread = key row: P^T and dS^T for queries 0..63; then dV out
+//   warps 8-11  thread = key row: P^T and dS^T for queries 64..127; then dK out
 // Tensor memory (512 columns): [0,128) S^T, [128,256) dP^T, then dV and dK
-// (d columns each). With d = 128 the dQ^T partial (d lanes x 128 queries)
-// reuses the dP^T columns once dS^T has been formed; with d = 64 the dQ
-// partial (128 queries x 64) has its own columns at 384.
-// Shared memory: K_j, V_j, Q_i[2], dO_i[2], one bf16 [keys][queries] tile that
-// holds P^T and then dS^T of the current step, LSE and D of the current step.
+// (d columns each). Shared memory: K_j, V_j, Q_i[2], dO_i[2], one bf16
+// [keys][queries] tile that holds P^T and then dS^T of the current step, and
+// LSE and D of the current step. MMA order per step n: dV(n), S^T(n+1),
+// dK(n), dP^T(n+1), so that the P^T/dS^T work of one step overlaps the
+// tensor core's work on the neighbouring steps.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -41,7 +45,7 @@ namespace {
 constexpr int kThreads = 384;
 
 template <int D>
-struct BwdLayout {
+struct DkdvLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
@@ -49,19 +53,16 @@ struct BwdLayout {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;       // 2 stages
   static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // 2 stages
-  static constexpr int kDSOff = kdOOff + 2 * kTileBytes; // bf16 [128 keys][128 queries]
-  static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int kStatOff = kDSOff + kDSBytes;     // [2 stages][lse2 128 | delta 128] fp32
+  static constexpr int kPSOff = kdOOff + 2 * kTileBytes; // bf16 [128 keys][128 queries]
+  static constexpr int kPSBytes = kTile * kTile * 2;
+  static constexpr int kStatOff = kPSOff + kPSBytes;     // [2 stages][lse2 128 | delta 128] fp32
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kBarOff = kStatOff + 2 * kStatBytes;
   static constexpr int kNumBars = 14;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
-  // tensor memory columns
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static constexpr bool kDqAlias = (D == 128);          // dQ^T in the dP^T columns
-  static constexpr uint32_t kColDQ = kDqAlias ? kColDP : 384;
 };
 
 struct Bars {
@@ -74,13 +75,12 @@ struct Bars {
   __device__ uint32_t dp_full() const { return base + 8 * 7; }
   __device__ uint32_t dv_done() const { return base + 8 * 8; }
   __device__ uint32_t ds_full() const { return base + 8 * 9; }
-  __device__ uint32_t dq_full() const { return base + 8 * 10; }
-  __device__ uint32_t dq_free() const { return base + 8 * 11; }
-  __device__ uint32_t acc_done() const { return base + 8 * 12; }
-  __device__ uint32_t teardown() const { return base + 8 * 13; }
+  __device__ uint32_t dk_done() const { return base + 8 * 10; }
+  __device__ uint32_t acc_done() const { return base + 8 * 11; }
+  __device__ uint32_t teardown() const { return base + 8 * 12; }
 };
 
-enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleDq = 4, kRoleInit = 5 };
+enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
 
 // Next Q tile at or after i that sees K/V tile j (T if none).
 __device__ __forceinline__ int next_q(const BwdParams &p, int i, int j, int T) {
@@ -89,14 +89,22 @@ __device__ __forceinline__ int next_q(const BwdParams &p, int i, int j, int T) {
   return i;
 }
 
-__device__ __forceinline__ uint32_t ds_addr(uint32_t base, int row, int unit16) {
+__device__ __forceinline__ uint32_t ps_addr(uint32_t base, int row, int unit16) {
   // bf16 [row][128 cols] as two 64-column chunks, 128-byte swizzle
   return base + (unit16 >> 3) * (kTile * 128) + row * 128 + (((unit16 & 7) ^ (row & 7)) << 4);
 }
 
+__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
-  using L = BwdLayout<D>;
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant__ BwdParams p) {
+  using L = DkdvLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort
@@ -108,17 +116,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
   }
   const uint32_t sK = s_base + L::kKOff, sV = s_base + L::kVOff;
   const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff;
-  const uint32_t sDS = s_base + L::kDSOff;
+  const uint32_t sPS = s_base + L::kPSOff;
   const float *stat = reinterpret_cast<const float *>(smem + L::kStatOff);
   Bars bars{s_base + L::kBarOff};
   StatusSlot st{p.status, &misc[2]};
 
   const int warp = threadIdx.x >> 5;
   const int T = p.n / kTile;
-  // CTAs are ordered head group by head group (p.head_group heads at a time),
-  // so that the fp32 dQ rows being accumulated by concurrent CTAs stay in L2;
-  // within a group the heavy K/V tiles come first (causal: tile j sees T - j
-  // Q tiles).
+  // CTAs are ordered head group by head group (p.head_group heads at a
+  // time); within a group the heavy K/V tiles come first (causal: tile j is
+  // seen by T - j Q tiles).
   const int hg = p.head_group;
   const int group = blockIdx.x / (hg * T);
   const int g_base = group * hg;
@@ -137,12 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
       mbar_init(bars.q_empty(s), 1);
     }
     mbar_init(bars.s_full(), 1);
-    mbar_init(bars.p_full(), 128);
+    mbar_init(bars.p_full(), 256);
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.dv_done(), 1);
-    mbar_init(bars.ds_full(), 128);
-    mbar_init(bars.dq_full(), 1);
-    mbar_init(bars.dq_free(), 128);
+    mbar_init(bars.ds_full(), 256);
+    mbar_init(bars.dk_done(), 1);
     mbar_init(bars.acc_done(), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
@@ -200,95 +206,63 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
     if (elect_one()) {
       constexpr uint32_t kIdSq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, 0, 1);     // dV, dK: B MN-major
-      // dQ^T = K^T dS^T (M = d) for d = 128; dQ = dS K (M = 128 queries) for d = 64
-      constexpr uint32_t kIdDq = L::kDqAlias ? idesc_bf16_f32(kTile, kTile, 1, 1)
-                                             : idesc_bf16_f32(kTile, D, 1, 1);
       bool ok = !any || mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleMma, 1));
-      // S^T(i) = K_j Q_i^T: both operands K-major over d
-      auto issue_s = [&](int s) {
-        const uint32_t q = sQ + s * L::kTileBytes;
+      // X^T = A Y^T with A in {K_j, V_j} and Y in {Q_i, dO_i}: K-major over d
+      auto issue_sq = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::kColS, sdesc_sw128(sK + off, 16, 1024),
-                      sdesc_sw128(q + off, 16, 1024), kIdSq, kk > 0);
+          mma_bf16_ss(tmem + col, sdesc_sw128(a_base + off, 16, 1024),
+                      sdesc_sw128(b_base + off, 16, 1024), kIdSq, kk > 0);
         }
       };
-      int n = 0;
+      // acc += P^T (or dS^T) Y: A = the shared [keys][queries] tile, K-major over
+      // queries; B = Y with queries as K (MN-major, 16 query rows per step)
+      auto issue_acc = [&](uint32_t y_base, uint32_t col, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + col, sdesc_sw128(sPS + a_off, 16, 1024),
+                      sdesc_sw128(y_base + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
+                      (!first || kk > 0) ? 1u : 0u);
+        }
+      };
       if (ok && any) {
         ok = mbar_wait(bars.q_full(0), 0, st, status_code(kKernBwd, kRoleMma, 2));
         if (ok) {
           tc_fence_after();
-          issue_s(0);
+          issue_sq(sK, sQ, L::kColS);
           mma_commit(bars.s_full());
+          issue_sq(sV, sdO, L::kColDP);
+          mma_commit(bars.dp_full());
         }
       }
+      int n = 0;
       for (int i = first; i < T && ok; ++n) {
-        const int s = n & 1;
+        const int s = n & 1, s1 = s ^ 1;
         const int inext = next_q(p, i + 1, j, T);
-        const uint32_t q = sQ + s * L::kTileBytes, dO = sdO + s * L::kTileBytes;
-        // dP^T = V_j dO_i^T (its columns hold the previous dQ^T when aliased)
-        if (L::kDqAlias && n > 0) {
-          ok = mbar_wait(bars.dq_free(), (n - 1) & 1, st, status_code(kKernBwd, kRoleMma, 3));
-          if (!ok) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(sV + off, 16, 1024),
-                      sdesc_sw128(dO + off, 16, 1024), kIdSq, kk > 0);
-        }
-        mma_commit(bars.dp_full());
-        // dV += P^T dO_i once P^T is in shared memory
-        ok = mbar_wait(bars.p_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 4));
+        ok = mbar_wait(bars.p_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(sDS + a_off, 16, 1024),
-                      sdesc_sw128(dO + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-        }
+        issue_acc(sdO + s * L::kTileBytes, L::kColDV, n == 0);
         mma_commit(bars.dv_done());
-        // S^T of the next Q tile, overlapping the dS^T work of this one
         if (inext < T) {
-          const int s1 = (n + 1) & 1;
-          ok = mbar_wait(bars.q_full(s1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 5));
+          ok = mbar_wait(bars.q_full(s1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 4));
           if (!ok) break;
           tc_fence_after();
-          issue_s(s1);
+          issue_sq(sK, sQ + s1 * L::kTileBytes, L::kColS);
           mma_commit(bars.s_full());
         }
-        // dK += dS^T Q_i and the dQ partial once dS^T is in shared memory
-        ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 6));
+        ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 5));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(sDS + a_off, 16, 1024),
-                      sdesc_sw128(q + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!L::kDqAlias && n > 0) {
-          ok = mbar_wait(bars.dq_free(), (n - 1) & 1, st, status_code(kKernBwd, kRoleMma, 7));
-          if (!ok) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // K dimension = keys: both operands are MN-major, 16 key rows per step
-          if (L::kDqAlias)
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(sK + kk * 2048, L::kChunkBytes, 1024),
-                        sdesc_sw128(sDS + kk * 2048, L::kChunkBytes, 1024), kIdDq, kk > 0);
-          else
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(sDS + kk * 2048, L::kChunkBytes, 1024),
-                        sdesc_sw128(sK + kk * 2048, L::kChunkBytes, 1024), kIdDq, kk > 0);
-        }
-        mma_commit(bars.dq_full());
+        issue_acc(sQ + s * L::kTileBytes, L::kColDK, n == 0);
+        mma_commit(bars.dk_done());
         mma_commit(bars.q_empty(s));
+        if (inext < T) {
+          issue_sq(sV, sdO + s1 * L::kTileBytes, L::kColDP);
+          mma_commit(bars.dp_full());
+        }
         i = inext;
       }
       if (ok) mma_commit(bars.acc_done());
@@ -296,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
       mbar_wait(bars.teardown(), 0, st, status_code(kKernBwd, kRoleMma, 8));
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // ---- P^T and dS^T (thread = key row) -----------------------------------
-    const int kr = threadIdx.x - 128;
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+  } else if (warp >= 4) {
+    // ---- P^T and dS^T for one half of the queries (thread = key row) --------
+    const int h = (warp - 4) >> 2;                 // query half: 64h .. 64h+63
+    const int kr = threadIdx.x & 127;              // key row = TMEM lane
+    const uint32_t t = tmem + (uint32_t((warp & 3) * 32) << 16);
     const float c = p.scale_log2;
     bool ok = true;
     int n = 0;
@@ -311,167 +286,89 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
                                                      status_code(kKernBwd, kRoleSoftmax, 2)));
       if (!ok) break;
       tc_fence_after();
-      const float *lse2 = stat + s * 2 * kTile;
+      const float *lse2 = stat + s * 2 * kTile + 64 * h;
       const float *delta = lse2 + kTile;
-      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); hidden entries 0.
-      // S^T is read 32 columns at a time to keep register pressure low.
+      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); key kr sees query
+      // q only if kr <= q on the diagonal tile of causal attention
       const bool diag = p.causal && i == j;
-      uint32_t pk[64];
+      float pr[64];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t sr[32];
-        tmem_ld32(tmem + lane_off + L::kColS + q * 32, sr);
-        tmem_wait_ld();
+      for (int q = 0; q < 2; ++q) {
+        float sv[32];
+        ld_cols32(t + L::kColS + 64 * h + 32 * q, sv);
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int col = 32 * q + x;
-          const float2 l2 = *reinterpret_cast<const float2 *>(lse2 + col);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[x]), c, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[x + 1]), c, -l2.y));
-          if (diag) {
-            if (col < kr) p0 = 0.f;
-            if (col + 1 < kr) p1 = 0.f;
-          }
-          pk[col >> 1] = pack_bf16x2(p0, p1);
+        for (int x = 0; x < 32; ++x) {
+          const int col = 64 * h + 32 * q + x;
+          float v = ex2_approx(fmaf(sv[x], c, -lse2[32 * q + x]));
+          pr[32 * q + x] = (diag && col < kr) ? 0.f : v;
         }
       }
-      // the shared P^T/dS^T tile is free once the previous dK/dQ MMAs are done
+      // the shared tile is free once dK of the previous step has read dS^T
       if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_full(), (n - 1) & 1, st,
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.dk_done(), (n - 1) & 1, st,
                                                status_code(kKernBwd, kRoleSoftmax, 3)));
         if (!ok) break;
       }
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        st_shared_v4(ds_addr(sDS, kr, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(ps_addr(sPS, kr, 8 * h + u), pack_bf16x2(pr[8 * u], pr[8 * u + 1]),
+                     pack_bf16x2(pr[8 * u + 2], pr[8 * u + 3]),
+                     pack_bf16x2(pr[8 * u + 4], pr[8 * u + 5]),
+                     pack_bf16x2(pr[8 * u + 6], pr[8 * u + 7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.p_full());
       // dS^T_kq = P^T_kq (dP^T_kq - D_q), written over P^T once dV has read it
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 4)));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bars.dv_done(), n & 1, st,
-                                                     status_code(kKernBwd, kRoleSoftmax, 5)));
       if (!ok) break;
       tc_fence_after();
+      uint32_t dsp[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + L::kColDP + q * 32, dp);
-        tmem_wait_ld();
+      for (int q = 0; q < 2; ++q) {
+        float dp[32];
+        ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 16-byte unit 4q+u: queries 32q+8u .. +7
-          uint32_t w[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int x = 32 * q + 8 * u + 2 * h;
-            const uint32_t pp = pk[x >> 1];
-            const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
-            const float d0 = p0 * (__uint_as_float(dp[8 * u + 2 * h]) - delta[x]);
-            const float d1 = p1 * (__uint_as_float(dp[8 * u + 2 * h + 1]) - delta[x + 1]);
-            w[h] = pack_bf16x2(d0, d1);
-          }
-          st_shared_v4(ds_addr(sDS, kr, 4 * q + u), w[0], w[1], w[2], w[3]);
-        }
+        for (int x = 0; x < 32; x += 2)
+          dsp[16 * q + x / 2] = pack_bf16x2(pr[32 * q + x] * (dp[x] - delta[32 * q + x]),
+                                            pr[32 * q + x + 1] * (dp[x + 1] - delta[32 * q + x + 1]));
       }
-      fence_proxy_async_smem();
       tc_fence_before();
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.dv_done(), n & 1, st,
+                                             status_code(kKernBwd, kRoleSoftmax, 5)));
+      if (!ok) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(ps_addr(sPS, kr, 8 * h + u), dsp[4 * u], dsp[4 * u + 1], dsp[4 * u + 2],
+                     dsp[4 * u + 3]);
+      fence_proxy_async_smem();
       mbar_arrive(bars.ds_full());
     }
-    // epilogue: dV rows of this K/V tile
+    // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled)
     if (ok && any)
       ok = __all_sync(0xffffffffu, mbar_wait(bars.acc_done(), 0, st,
                                              status_code(kKernBwd, kRoleSoftmax, 6)));
     if (ok) {
       tc_fence_after();
-      uint16_t *dst_row = static_cast<uint16_t *>(p.dv) + (kvrow + kr) * D;
+      const uint32_t col = h ? L::kColDK : L::kColDV;
+      const float sc = h ? p.scale : 1.f;
+      uint16_t *dst_row = static_cast<uint16_t *>(h ? p.dk : p.dv) + (kvrow + kr) * D;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
+        float v[32];
         if (any) {
-          tmem_ld32(tmem + lane_off + L::kColDV + q * 32, v);
-          tmem_wait_ld();
+          ld_cols32(t + col + q * 32, v);
         } else {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0u;
+          for (int x = 0; x < 32; ++x) v[x] = 0.f;
         }
         uint4 *dst = reinterpret_cast<uint4 *>(dst_row + q * 32);
 #pragma unroll
         for (int x = 0; x < 4; ++x)
-          dst[x] = make_uint4(
-              pack_bf16x2(__uint_as_float(v[8 * x + 0]), __uint_as_float(v[8 * x + 1])),
-              pack_bf16x2(__uint_as_float(v[8 * x + 2]), __uint_as_float(v[8 * x + 3])),
-              pack_bf16x2(__uint_as_float(v[8 * x + 4]), __uint_as_float(v[8 * x + 5])),
-              pack_bf16x2(__uint_as_float(v[8 * x + 6]), __uint_as_float(v[8 * x + 7])));
-      }
-    }
-  } else if (warp >= 8) {
-    // ---- dQ partials -> fp32 reductions; then dK rows ------------------------
-    const int ln = threadIdx.x - 256;  // TMEM lane
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    bool ok = true;
-    int n = 0;
-    for (int i = first; i < T && ok; i = next_q(p, i + 1, j, T), ++n) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_full(), n & 1, st,
-                                             status_code(kKernBwd, kRoleDq, 1)));
-      if (!ok) break;
-      tc_fence_after();
-      const size_t qrow = (size_t)bh * p.n + (size_t)i * kTile;
-      if (L::kDqAlias) {
-        // lane = d index, columns = the 128 queries: one 128-byte line per warp and query
-        float *acc = p.dq_acc + qrow * D + ln;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + L::kColDQ + q * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) atomicAdd(acc + (size_t)(32 * q + x) * D, __uint_as_float(v[x]));
-        }
-      } else {
-        // lane = query row, columns = d
-        float4 *acc = reinterpret_cast<float4 *>(p.dq_acc + (qrow + ln) * D);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + L::kColDQ + q * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 8; ++x)
-            atomicAdd(acc + q * 8 + x,
-                      make_float4(__uint_as_float(v[4 * x]), __uint_as_float(v[4 * x + 1]),
-                                  __uint_as_float(v[4 * x + 2]), __uint_as_float(v[4 * x + 3])));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bars.dq_free());
-    }
-    // epilogue: dK rows of this K/V tile (scaled)
-    if (ok && any)
-      ok = __all_sync(0xffffffffu, mbar_wait(bars.acc_done(), 0, st,
-                                             status_code(kKernBwd, kRoleDq, 2)));
-    if (ok) {
-      tc_fence_after();
-      uint16_t *dst_row = static_cast<uint16_t *>(p.dk) + (kvrow + ln) * D;
-      const float sc = p.scale;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        if (any) {
-          tmem_ld32(tmem + lane_off + L::kColDK + q * 32, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0u;
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + q * 32);
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-          dst[x] = make_uint4(
-              pack_bf16x2(__uint_as_float(v[8 * x + 0]) * sc, __uint_as_float(v[8 * x + 1]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * x + 2]) * sc, __uint_as_float(v[8 * x + 3]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * x + 4]) * sc, __uint_as_float(v[8 * x + 5]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * x + 6]) * sc, __uint_as_float(v[8 * x + 7]) * sc));
+          dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
+                              pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
+                              pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
+                              pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
       }
     }
   }
@@ -484,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_main(const __grid_constant
   }
 }
 
-// D_i = dO_i . O_i, LSE_i * log2(e) (0 for a row that sees no key), zero dQ_acc.
+// D_i = dO_i . O_i and LSE_i * log2(e) (0 for a row that sees no key).
 // Thread = 8 consecutive elements of a row (16-byte loads).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdParams p) {
@@ -503,9 +400,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
       acc = fmaf(__uint_as_float(ow[h] << 16), __uint_as_float(gw[h] << 16), acc);
       acc = fmaf(__uint_as_float(ow[h] & 0xffff0000u), __uint_as_float(gw[h] & 0xffff0000u), acc);
     }
-    float4 *z = reinterpret_cast<float4 *>(p.dq_acc + row * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -516,25 +410,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
   }
 }
 
-// dQ = bf16(scale * dQ_acc), 8 elements per thread.
-__global__ void __launch_bounds__(256) fa_bwd_dq(const __grid_constant__ BwdParams p) {
-  const size_t total8 = (size_t)p.bh * p.n * p.d / 8;
-  const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gt >= total8) return;
-  const float4 *src = reinterpret_cast<const float4 *>(p.dq_acc) + 2 * gt;
-  const float4 a = src[0], b = src[1];
-  const float sc = p.scale;
-  reinterpret_cast<uint4 *>(p.dq)[gt] =
-      make_uint4(pack_bf16x2(a.x * sc, a.y * sc), pack_bf16x2(a.z * sc, a.w * sc),
-                 pack_bf16x2(b.x * sc, b.y * sc), pack_bf16x2(b.z * sc, b.w * sc));
-}
-
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
-  using L = BwdLayout<D>;
+  using L = DkdvLayout<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kBytes);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -545,17 +426,15 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     LaunchProbe probe(kKindBwdPre, stream);
     fa_bwd_pre<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, stream>>>(p);
   }
-  const int T = p.n / kTile;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   {
-    LaunchProbe probe(kKindBwdMain, stream);
-    fa_bwd_main<D><<<T * p.bh, kThreads, L::kBytes, stream>>>(p);
+    LaunchProbe probe(kKindBwdDkdv, stream);
+    fa_bwd_dkdv<D><<<(p.n / kTile) * p.bh, kThreads, L::kBytes, stream>>>(p);
   }
-  const size_t total8 = rows * D / 8;
-  {
-    LaunchProbe probe(kKindBwdDq, stream);
-    fa_bwd_dq<<<(unsigned)((total8 + 255) / 256), 256, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_backward_dq(p, stream);
 }
 
 }  // namespace

@@ -28,7 +28,6 @@ struct BwdParams {
   const float *lse;                   // [B*H*N]
   float *delta;                       // workspace: D_i [B*H*N]
   float *lse2;                        // workspace: LSE_i * log2(e) [B*H*N]
-  float *dq_acc;                      // workspace: fp32 [B*H*N][d]
   void *dq, *dk, *dv;                 // bf16 outputs
   const uint8_t *mask;
   int bh, n, d, causal;
@@ -38,7 +37,7 @@ struct BwdParams {
 };
 
 // Kernel ids of the measurement hooks (names in fa_kernel_name()).
-enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdDq = 3,
+enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdDkdv = 2, kKindBwdDq = 3,
                         kNumKinds = 4 };
 
 // Brackets one launch with CUDA events when measurement is enabled
@@ -54,6 +53,7 @@ class LaunchProbe {
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
+cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_bwd_dq.cu
 
 // Status word codes: 0x80000000 | kernel << 16 | role << 8 | site.
 enum KernelId : uint32_t { kKernFwd = 1, kKernBwdPre = 2, kKernBwd = 3, kKernBwdDq = 4 };

@@ -93,9 +93,9 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
                          const uint8_t *block_mask, void *stream);
 
 /*
- * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i),
- * fp32 LSE*log2(e) [B,H,N] and an fp32 dQ accumulator [B,H,N,d], each
- * starting on a 256-byte boundary. Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i)
+ * and fp32 LSE*log2(e) [B,H,N], each starting on a 256-byte boundary: O(N),
+ * 8 bytes per query row. Returns 0 for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 

@@ -34,7 +34,7 @@ def _p(t):
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     """Validation happens before any CUDA call, so this runs without a GPU."""
     fake = ctypes.c_void_p(0x10000)
-    B, H, N, d = 4, 16, 4096, 128
+    B, H, N, d = 512, 64, 8192, 128  # 2^28 query rows: 2 GiB of row statistics
     assert lib.fa_backward_workspace_bytes(B, H, N, d) > lib.fa_backward_noalloc_max_bytes()
     rc = lib.fa_backward_noalloc(*([fake] * 9), B, H, N, d, 1, 0.088, None, None)
     assert rc == 2  # FA_ERR_UNSUPPORTED
