@@ -22,6 +22,7 @@
 //   warps 8-11  softmax of Q tile 1
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S_0   [128,256) S_1   [256,256+d) O_0   [256+d,256+2d) O_1
+//   P_t (bf16 pairs): the first 64 columns of S_t (d = 128) or [384+64t, +64) (d = 64)
 // The MMA issue order PV_0(n), S_0(n+1), PV_1(n), S_1(n+1) lets the tensor
 // core work on one Q tile while the other tile's softmax runs.
 #include <math.h>
@@ -40,12 +41,10 @@ struct FwdLayout {
   static constexpr int kChunks = D / 64;              // 128-byte column chunks per row
   static constexpr int kChunkBytes = kTile * 128;     // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring slots (K and V alternate)
-  static constexpr int kPBytes = kTile * kTile * 2;   // bf16 P tile, 2 chunks of 64 keys
+  static constexpr int kStages = (D == 128) ? 5 : 10;  // K/V ring slots (K and V alternate)
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
-  static constexpr int kPOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kListOff = kPOff + 2 * kPBytes;
+  static constexpr int kListOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, teardown
   static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
@@ -53,6 +52,11 @@ struct FwdLayout {
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
   static_assert(kAlloc <= 232448, "shared memory budget");
+  // P_t (bf16 pairs, 64 columns) lives in tensor memory as the A operand of
+  // O_t += P_t V. With d = 128 the 512 columns hold S_0, S_1, O_0, O_1 and P_t
+  // takes the first half of S_t's columns once S_t has been read; with d = 64
+  // it has columns of its own.
+  __host__ __device__ static constexpr uint32_t col_p(int t) { return D == 128 ? t * kTile : 384 + 64 * t; }
 };
 
 struct Bars {
@@ -82,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ = s_base + L::kQOff;
   const uint32_t sKV = s_base + L::kKVOff;
-  const uint32_t sP = s_base + L::kPOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort
   Bars bars{s_base + L::kBarOff, L::kStages};
@@ -204,16 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                       sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
         }
       };
+      // O_t += P_t V: A = P_t from tensor memory (8 columns per 16 keys),
+      // B = V with keys as K (MN-major, 16 key rows per step). With d = 128,
+      // S_t(n+1) is issued after this MMA into the columns P_t occupies; MMAs
+      // issued by one thread execute in issue order, so P_t is read first.
       auto issue_pv = [&](int t, int vslot, bool first) {
-        const uint32_t p_base = sP + t * L::kPBytes;
         const uint32_t v_base = sKV + vslot * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 256 + t * D, sdesc_sw128(p_base + a_off, 16, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
                       sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
                       (kk > 0 || !first) ? 1u : 0u);
-        }
       };
 
       if (ok && count > 0) {
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * kTile;
     const uint32_t tO = tmem + lane_off + 256 + t * D;
-    const uint32_t p_row = sP + t * L::kPBytes + r * 128;
+    const uint32_t tP = tmem + lane_off + L::col_p(t);
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     uint32_t scount = 0;
@@ -315,22 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         l *= alpha;
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-        // P = exp2(s*c - m) -> bf16, written K-major with the 128-byte swizzle
+        // P = exp2(s*c - m) -> bf16 pairs (keys 2x, 2x+1 in column x) in tensor memory
+        uint32_t pk0[32], pk1[32];
 #pragma unroll
-        for (int u = 0; u < kTile / 8; ++u) {  // 16-byte unit u holds keys 8u..8u+7
-          uint32_t pk[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float p0 = ex2_approx(fmaf(s[8 * u + 2 * h], c, -m_sub));
-            const float p1 = ex2_approx(fmaf(s[8 * u + 2 * h + 1], c, -m_sub));
-            l += p0 + p1;
-            pk[h] = pack_bf16x2(p0, p1);
-          }
-          const uint32_t chunk = u >> 3, unit = u & 7;
-          st_shared_v4(p_row + chunk * L::kChunkBytes + ((unit ^ (r & 7)) << 4), pk[0], pk[1],
-                       pk[2], pk[3]);
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = ex2_approx(fmaf(s[2 * x], c, -m_sub));
+          const float p1 = ex2_approx(fmaf(s[2 * x + 1], c, -m_sub));
+          l += p0 + p1;
+          pk0[x] = pack_bf16x2(p0, p1);
         }
-        fence_proxy_async_smem();
+        tmem_st32(tP, pk0);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
+          const float p1 = ex2_approx(fmaf(s[64 + 2 * x + 1], c, -m_sub));
+          l += p0 + p1;
+          pk1[x] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tP + 32, pk1);
         if (any && __any_sync(0xffffffffu, need)) {
           // O *= alpha for this row. The PV MMA of the previous tile has
           // completed: it was issued before this S tile, whose completion we
@@ -344,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
             tmem_st16(tO + q * 16, o);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();  // P (and a rescaled O) are in tensor memory
         tc_fence_before();
         mbar_arrive(bars.p_full(t));
         any = true;
