@@ -29,11 +29,14 @@
 //   warps 4-7   thread = key row: P^T and dS^T for queries 0..63; then dV out
 //   warps 8-11  thread = key row: P^T and dS^T for queries 64..127; then dK out
 // Tensor memory (512 columns): [0,128) S^T, [128,256) dP^T, then dV and dK
-// (d columns each). Shared memory: K_j, V_j, Q_i[2], dO_i[2], one bf16
-// [keys][queries] tile that holds P^T and then dS^T of the current step, and
+// (d columns each). P^T and dS^T (bf16 pairs) are the tensor-memory A
+// operands of dV += P^T dO and dK += dS^T Q: the warpgroup for queries
+// 64h..64h+63 writes them over the first 32 of its own 64 S^T (dP^T)
+// columns once it has read them. Shared memory: K_j, V_j, Q_i[2], dO_i[2],
 // LSE and D of the current step. MMA order per step n: dV(n), S^T(n+1),
-// dK(n), dP^T(n+1), so that the P^T/dS^T work of one step overlaps the
-// tensor core's work on the neighbouring steps.
+// dK(n), dP^T(n+1); MMAs issued by one thread execute in issue order, so
+// S^T(n+1) and dP^T(n+1) overwrite P^T(n) and dS^T(n) only after dV(n) and
+// dK(n) have read them.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -53,9 +56,7 @@ struct DkdvLayout {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;       // 2 stages
   static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // 2 stages
-  static constexpr int kPSOff = kdOOff + 2 * kTileBytes; // bf16 [128 keys][128 queries]
-  static constexpr int kPSBytes = kTile * kTile * 2;
-  static constexpr int kStatOff = kPSOff + kPSBytes;     // [2 stages][lse2 128 | delta 128] fp32
+  static constexpr int kStatOff = kdOOff + 2 * kTileBytes; // [2 stages][lse2 128 | delta 128] fp32
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kBarOff = kStatOff + 2 * kStatBytes;
   static constexpr int kNumBars = 14;
@@ -73,9 +74,7 @@ struct Bars {
   __device__ uint32_t s_full() const { return base + 8 * 5; }
   __device__ uint32_t p_full() const { return base + 8 * 6; }
   __device__ uint32_t dp_full() const { return base + 8 * 7; }
-  __device__ uint32_t dv_done() const { return base + 8 * 8; }
   __device__ uint32_t ds_full() const { return base + 8 * 9; }
-  __device__ uint32_t dk_done() const { return base + 8 * 10; }
   __device__ uint32_t acc_done() const { return base + 8 * 11; }
   __device__ uint32_t teardown() const { return base + 8 * 12; }
 };
@@ -89,10 +88,9 @@ __device__ __forceinline__ int next_q(const BwdParams &p, int i, int j, int T) {
   return i;
 }
 
-__device__ __forceinline__ uint32_t ps_addr(uint32_t base, int row, int unit16) {
-  // bf16 [row][128 cols] as two 64-column chunks, 128-byte swizzle
-  return base + (unit16 >> 3) * (kTile * 128) + row * 128 + (((unit16 & 7) ^ (row & 7)) << 4);
-}
+// Tensor-memory column of the packed A operand (P^T or dS^T) for MMA step kk
+// (queries 16kk..16kk+15): queries 64h.. are packed at column 64h.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -116,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   }
   const uint32_t sK = s_base + L::kKOff, sV = s_base + L::kVOff;
   const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff;
-  const uint32_t sPS = s_base + L::kPSOff;
   const float *stat = reinterpret_cast<const float *>(smem + L::kStatOff);
   Bars bars{s_base + L::kBarOff};
   StatusSlot st{p.status, &misc[2]};
@@ -146,9 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.p_full(), 256);
     mbar_init(bars.dp_full(), 1);
-    mbar_init(bars.dv_done(), 1);
     mbar_init(bars.ds_full(), 256);
-    mbar_init(bars.dk_done(), 1);
     mbar_init(bars.acc_done(), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
@@ -216,16 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
                       sdesc_sw128(b_base + off, 16, 1024), kIdSq, kk > 0);
         }
       };
-      // acc += P^T (or dS^T) Y: A = the shared [keys][queries] tile, K-major over
-      // queries; B = Y with queries as K (MN-major, 16 query rows per step)
-      auto issue_acc = [&](uint32_t y_base, uint32_t col, bool first) {
+      // acc += X Y with X = P^T (or dS^T) packed in tensor memory at a_col and
+      // Y with queries as K (MN-major, 16 query rows per step)
+      auto issue_acc = [&](uint32_t a_col, uint32_t y_base, uint32_t col, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + col, sdesc_sw128(sPS + a_off, 16, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + col, tmem + a_col + packed_col(kk),
                       sdesc_sw128(y_base + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
                       (!first || kk > 0) ? 1u : 0u);
-        }
       };
       if (ok && any) {
         ok = mbar_wait(bars.q_full(0), 0, st, status_code(kKernBwd, kRoleMma, 2));
@@ -244,8 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         ok = mbar_wait(bars.p_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(sdO + s * L::kTileBytes, L::kColDV, n == 0);
-        mma_commit(bars.dv_done());
+        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0);
         if (inext < T) {
           ok = mbar_wait(bars.q_full(s1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 4));
           if (!ok) break;
@@ -256,8 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 5));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(sQ + s * L::kTileBytes, L::kColDK, n == 0);
-        mma_commit(bars.dk_done());
+        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0);
         mma_commit(bars.q_empty(s));
         if (inext < T) {
           issue_sq(sV, sdO + s1 * L::kTileBytes, L::kColDP);
@@ -303,22 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
           pr[32 * q + x] = (diag && col < kr) ? 0.f : v;
         }
       }
-      // the shared tile is free once dK of the previous step has read dS^T
-      if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.dk_done(), (n - 1) & 1, st,
-                                               status_code(kKernBwd, kRoleSoftmax, 3)));
-        if (!ok) break;
-      }
+      // P^T into tensor memory over this warpgroup's first 32 S^T columns
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(ps_addr(sPS, kr, 8 * h + u), pack_bf16x2(pr[8 * u], pr[8 * u + 1]),
-                     pack_bf16x2(pr[8 * u + 2], pr[8 * u + 3]),
-                     pack_bf16x2(pr[8 * u + 4], pr[8 * u + 5]),
-                     pack_bf16x2(pr[8 * u + 6], pr[8 * u + 7]));
-      fence_proxy_async_smem();
+        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(pr[2 * x], pr[2 * x + 1]);
+        tmem_st32(t + L::kColS + 64 * h, pk);
+        tmem_wait_st();
+      }
       tc_fence_before();
       mbar_arrive(bars.p_full());
-      // dS^T_kq = P^T_kq (dP^T_kq - D_q), written over P^T once dV has read it
+      // dS^T_kq = P^T_kq (dP^T_kq - D_q) into tensor memory over dP^T
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 4)));
       if (!ok) break;
@@ -333,15 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
           dsp[16 * q + x / 2] = pack_bf16x2(pr[32 * q + x] * (dp[x] - delta[32 * q + x]),
                                             pr[32 * q + x + 1] * (dp[x + 1] - delta[32 * q + x + 1]));
       }
+      tmem_st32(t + L::kColDP + 64 * h, dsp);
+      tmem_wait_st();
       tc_fence_before();
-      ok = __all_sync(0xffffffffu, mbar_wait(bars.dv_done(), n & 1, st,
-                                             status_code(kKernBwd, kRoleSoftmax, 5)));
-      if (!ok) break;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(ps_addr(sPS, kr, 8 * h + u), dsp[4 * u], dsp[4 * u + 1], dsp[4 * u + 2],
-                     dsp[4 * u + 3]);
-      fence_proxy_async_smem();
       mbar_arrive(bars.ds_full());
     }
     // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled)
