@@ -307,9 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int x = 0; x < kTile; ++x)
             if (x > r) s[x] = -INFINITY;
         }
-        float mx = s[0];
+        // row max with 4 independent partial maxima (short dependency chains)
+        float mp[4];
 #pragma unroll
-        for (int x = 1; x < kTile; ++x) mx = fmaxf(mx, s[x]);
+        for (int x = 0; x < 4; ++x) mp[x] = s[x];
+#pragma unroll
+        for (int x = 4; x < kTile; ++x) mp[x & 3] = fmaxf(mp[x & 3], s[x]);
+        const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
         const float m_tile = mx * c;
         const bool need = m_tile > m_used + kRescaleThreshold;
         float alpha = 1.f;
@@ -317,15 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           alpha = ex2_approx(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
           m_used = m_tile;
         }
-        l *= alpha;
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-        // P = exp2(s*c - m) -> bf16 pairs (keys 2x, 2x+1 in column x) in tensor memory
+        // P = exp2(s*c - m) -> bf16 pairs (keys 2x, 2x+1 in column x) in tensor
+        // memory; the row sum uses 4 independent partial sums
+        float lp[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk0[32], pk1[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const float p0 = ex2_approx(fmaf(s[2 * x], c, -m_sub));
           const float p1 = ex2_approx(fmaf(s[2 * x + 1], c, -m_sub));
-          l += p0 + p1;
+          lp[x & 3] += p0 + p1;
           pk0[x] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tP, pk0);
@@ -333,10 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int x = 0; x < 32; ++x) {
           const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
           const float p1 = ex2_approx(fmaf(s[64 + 2 * x + 1], c, -m_sub));
-          l += p0 + p1;
+          lp[x & 3] += p0 + p1;
           pk1[x] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tP + 32, pk1);
+        l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
         if (any && __any_sync(0xffffffffu, need)) {
           // O *= alpha for this row. The PV MMA of the previous tile has
           // completed: it was issued before this S tile, whose completion we
