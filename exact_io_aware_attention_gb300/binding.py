@@ -35,6 +35,7 @@ SIGNATURES = {
     "fa_backward_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_backward_noalloc_max_bytes": ([], _sz),
     "fa_device_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i),
+    "fa_debug_configure": ([ctypes.c_uint, ctypes.c_ulonglong], _i),
     "fa_num_kernels": ([], _i),
     "fa_kernel_name": ([_i], ctypes.c_char_p),
     "fa_profile_enable": ([_i], _i),

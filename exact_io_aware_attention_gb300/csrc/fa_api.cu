@@ -20,6 +20,10 @@ namespace {
 // Device status word written by kernel-side bounded waits that give up.
 __device__ unsigned int g_status_word = 0u;
 
+// Process-wide debug settings (fa_debug_configure).
+std::atomic<uint32_t> g_debug_flags{0};
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the default limit
+
 // Text of the last FA_ERR_CUDA failure of the calling thread.
 thread_local char g_last_error[256] = "";
 
@@ -149,6 +153,8 @@ fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, flo
   p.causal = causal ? 1 : 0;
   p.o_f32 = o_f32;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  p.debug_flags = g_debug_flags.load();
+  p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
   e = fa::launch_forward(p, static_cast<cudaStream_t>(stream));
@@ -345,6 +351,8 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.head_group = backward_head_group(p.bh);
+  p.debug_flags = g_debug_flags.load();
+  p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
   e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));
@@ -367,6 +375,13 @@ fa_status fa_device_status(void *stream, unsigned int *code) {
 }
 
 const char *fa_last_error(void) { return g_last_error; }
+
+fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_ns) {
+  if (flags & ~fa::kDebugSkipLoads) return FA_ERR_INVALID_ARG;
+  g_debug_flags.store(flags);
+  g_wait_limit_ns.store(wait_limit_ns);
+  return FA_OK;
+}
 
 size_t fa_backward_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
 

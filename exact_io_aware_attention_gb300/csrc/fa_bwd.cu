@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff;
   const float *stat = reinterpret_cast<const float *>(smem + L::kStatOff);
   Bars bars{s_base + L::kBarOff};
-  StatusSlot st{p.status, &misc[2]};
+  StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
   const int warp = threadIdx.x >> 5;
   const int T = p.n / kTile;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
-    if (elect_one() && any) {
+    if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.kv_full(), 2 * L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c) {
         tma_load_2d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, (int)kvrow, bars.kv_full());

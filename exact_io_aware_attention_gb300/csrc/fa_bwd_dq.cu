@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   const uint32_t sK = s_base + L::kKOff, sV = s_base + L::kVOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
   Bars bars{s_base + L::kBarOff};
-  StatusSlot st{p.status, &misc[2]};
+  StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // CTA order: head groups of p.head_group heads; heavy Q tiles (late i for
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
 
   if (warp == 0) {
     // ---- TMA producer: Q, dO; then K_0, and per step K_{n+1}, V_n ------------
-    if (elect_one() && count > 0) {
+    if (elect_one() && count > 0 && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.q_full(), 2 * L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c) {
         tma_load_2d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0, bars.q_full());

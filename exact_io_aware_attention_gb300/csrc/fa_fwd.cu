@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort
   Bars bars{s_base + L::kBarOff, L::kStages};
-  StatusSlot st{p.status, &misc[2]};
+  StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
-    if (elect_one()) {
+    if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
       int pos = 0;
       bool ok = true;
       const uint32_t qbytes = (has1 ? 2u : 1u) * L::kTileBytes;

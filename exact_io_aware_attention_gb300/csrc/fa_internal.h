@@ -10,6 +10,7 @@ namespace fa {
 
 constexpr int kTile = 128;            // rows of a Q tile and keys of a K/V tile
 constexpr int kMaxTiles = 512;        // tiles per sequence the kernels accept (N <= 65536)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit of one kernel-side wait
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;       // 2-D bf16 maps [B*H*N rows][d], box 64 x 128, 128B swizzle
@@ -20,6 +21,8 @@ struct FwdParams {
   int o_f32;                          // 1: O stored as fp32
   float scale_log2;                   // scale * log2(e)
   unsigned int *status;               // device status word
+  uint32_t debug_flags;               // kDebug* bits (tests of the failure path only)
+  uint64_t wait_limit_ns;             // limit of one kernel-side wait
 };
 
 struct BwdParams {
@@ -34,6 +37,8 @@ struct BwdParams {
   int head_group;                     // CTA order: heads per group (1..bh)
   float scale, scale_log2;
   unsigned int *status;
+  uint32_t debug_flags;
+  uint64_t wait_limit_ns;
 };
 
 // Kernel ids of the measurement hooks (names in fa_kernel_name()).
@@ -50,6 +55,10 @@ class LaunchProbe {
   int slot_;
   cudaStream_t stream_;
 };
+
+// Debug flags (fa_debug_configure): the TMA producers issue no copy, so the
+// consumers' bounded waits run out and report through the status word.
+constexpr uint32_t kDebugSkipLoads = 1u;
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);

@@ -14,6 +14,7 @@ namespace fa {
 struct StatusSlot {
   unsigned int *word;   // global status word (per library), may be null
   int *abort_flag;      // shared-memory abort flag of this CTA
+  uint64_t limit_ns;    // wall-clock limit of one wait
 };
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -74,11 +75,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wall-clock limit of one wait. A healthy wait lasts microseconds; the limit
-// only turns a logic error into an error code instead of a hung GPU.
-#ifndef FA_WAIT_LIMIT_NS
-#define FA_WAIT_LIMIT_NS 2000000000ull
-#endif
+// The wall-clock limit of one wait comes with the status slot. A healthy wait
+// lasts microseconds; the limit only turns a logic error into an error code
+// instead of a hung GPU.
 
 // Waits for the phase of parity `parity` of barrier `bar` to complete.
 // Returns false (and records `code`) if it gives up or if another role of
@@ -90,7 +89,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*(volatile int *)st.abort_flag) return false;
-      if (global_timer_ns() - t0 > FA_WAIT_LIMIT_NS) {
+      if (global_timer_ns() - t0 > st.limit_ns) {
         *(volatile int *)st.abort_flag = 1;
         if (st.word) atomicCAS(st.word, 0u, code);
         return false;

@@ -154,6 +154,19 @@ size_t fa_backward_noalloc_max_bytes(void);
 fa_status fa_device_status(void *stream, unsigned int *code);
 
 /*
+ * Failure-path testing (process-wide; not for production use).
+ * flags = FA_DEBUG_SKIP_LOADS makes every kernel's TMA producer issue no
+ * copy, so the kernel's bounded waits run out: each CTA records
+ * 0x80000000 | kernel << 16 | role << 8 | site in the status word that
+ * fa_device_status() reads, frees its tensor memory and exits, and the CUDA
+ * context stays usable. wait_limit_ns sets the limit of one wait (0 restores
+ * the default of 2 s). fa_debug_configure(0, 0) restores normal operation.
+ * Returns FA_ERR_INVALID_ARG for unknown flag bits.
+ */
+#define FA_DEBUG_SKIP_LOADS 1u
+fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_ns);
+
+/*
  * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
  * 0 forward, 1 backward preprocess (D_i, LSE*log2 e, zeroed dQ accumulator),
  * 2 backward main, 3 backward dQ conversion; fa_kernel_name() names them
