@@ -7,8 +7,8 @@ input generators, which hold none of the method's arithmetic.
 
 The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, pthreads); this
 module compiles it with gcc and marshals numpy arrays to it. Every function
-takes and returns float64 arrays laid out ``[B, H, N, d]`` (statistics
-``[B, H, N]``).
+takes and returns float64 arrays: queries, outputs and their gradients laid out
+``[B, H, Nq, d]``, keys and values ``[B, H, Nk, d]``, statistics ``[B, H, Nq]``.
 
 What is computed, and which passage of the pages each part follows, is stated
 at the top of ``attn_oracle.c``. Parity status: every entry point is pinned by
@@ -54,14 +54,14 @@ def _load():
             ip = ctypes.POINTER(ctypes.c_int)
             up = ctypes.POINTER(ctypes.c_ubyte)
             i = ctypes.c_int
-            lib.oracle_forward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double,
-                                           up, i, ip, i, i]
+            lib.oracle_forward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i,
+                                           ctypes.c_double, up, i, ip, i, i]
             lib.oracle_forward.restype = i
-            lib.oracle_forward_tiled.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i,
+            lib.oracle_forward_tiled.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i,
                                                  ctypes.c_double, up, i, i, i, i]
             lib.oracle_forward_tiled.restype = i
             lib.oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i,
-                                            ctypes.c_double, up, i, ip, i, ip, i, i]
+                                            i, ctypes.c_double, up, i, ip, i, ip, i, i]
             lib.oracle_backward.restype = i
             _lib = lib
     return _lib
@@ -84,14 +84,26 @@ def _ptr(a, ctype=ctypes.c_double):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def _mask(block_mask, N, mask_tile):
+def _mask(block_mask, Nq, Nk, mask_tile):
     if block_mask is None:
         return None
     m = np.ascontiguousarray(np.asarray(block_mask, dtype=np.uint8))
-    T = (N + mask_tile - 1) // mask_tile
-    if m.shape != (T, T):
-        raise ValueError(f"block_mask must be [{T}, {T}] for N={N}, tile={mask_tile}")
+    Tq, Tk = (Nq + mask_tile - 1) // mask_tile, (Nk + mask_tile - 1) // mask_tile
+    if m.shape != (Tq, Tk):
+        raise ValueError(f"block_mask must be [{Tq}, {Tk}] for Nq={Nq}, Nk={Nk}, "
+                         f"tile={mask_tile}")
     return m
+
+
+def _shapes(q, kv, extra=()):
+    """(B, H, Nq, Nk, d) of queries q [B,H,Nq,d] and keys/values [B,H,Nk,d]."""
+    B, H, Nq, d = q.shape
+    Nk = kv[0].shape[2]
+    if any(t.shape != (B, H, Nk, d) for t in kv):
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
+    if any(t.shape != q.shape for t in extra):
+        raise ValueError("do must have q's shape")
+    return B, H, Nq, Nk, d
 
 
 def _idx(rows, N):
@@ -112,23 +124,22 @@ def forward(q, k, v, causal=False, scale=None, block_mask=None, mask_tile=128, r
             threads=None):
     """Exact attention from the definition: returns (O, LSE) in float64.
 
-    ``rows`` (optional) restricts the computation to those query rows; the
-    outputs are then ``[B, H, len(rows), d]`` and ``[B, H, len(rows)]``.
+    q is ``[B, H, Nq, d]``, k and v ``[B, H, Nk, d]``. ``rows`` (optional)
+    restricts the computation to those query rows; the outputs are then
+    ``[B, H, len(rows), d]`` and ``[B, H, len(rows)]``.
     """
     q, k, v = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
-    B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share one shape")
+    B, H, Nq, Nk, d = _shapes(q, (k, v))
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
-    m = _mask(block_mask, N, mask_tile)
-    r = _idx(rows, N)
-    nr = N if r is None else r.size
+    m = _mask(block_mask, Nq, Nk, mask_tile)
+    r = _idx(rows, Nq)
+    nr = Nq if r is None else r.size
     o = np.empty((B, H, nr, d), np.float64)
     lse = np.empty((B, H, nr), np.float64)
     if B * H * nr == 0:
         return o, lse
-    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte), mask_tile,
+    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk,
+                                d, int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte), mask_tile,
                                 _ptr(r, ctypes.c_int), nr, threads or default_threads())
     _check(rc, "oracle_forward")
     return o, lse
@@ -138,17 +149,15 @@ def forward_tiled(q, k, v, causal=False, scale=None, block_mask=None, mask_tile=
                   bk=64, threads=None):
     """The online-softmax recurrence over bq x bk blocks: returns (O, LSE)."""
     q, k, v = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
-    B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share one shape")
+    B, H, Nq, Nk, d = _shapes(q, (k, v))
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
-    m = _mask(block_mask, N, mask_tile)
-    o = np.empty((B, H, N, d), np.float64)
-    lse = np.empty((B, H, N), np.float64)
-    if B * H * N == 0:
+    m = _mask(block_mask, Nq, Nk, mask_tile)
+    o = np.empty((B, H, Nq, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    if B * H * Nq == 0:
         return o, lse
-    rc = _load().oracle_forward_tiled(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
-                                      d, int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte),
+    rc = _load().oracle_forward_tiled(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq,
+                                      Nk, d, int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte),
                                       mask_tile, int(bq), int(bk), threads or default_threads())
     _check(rc, "oracle_forward_tiled")
     return o, lse
@@ -158,29 +167,28 @@ def backward(q, k, v, do, causal=False, scale=None, block_mask=None, mask_tile=1
              qrows=None, kcols=None, want_dq=True, want_dkv=True, threads=None):
     """Analytic gradients of exact attention for upstream gradient ``do``.
 
-    Returns a dict with ``dq`` ([B,H,nq,d]), ``dk``/``dv`` ([B,H,nk,d]), and
-    ``lse``/``D`` ([B,H,N], the row statistics the oracle computed itself).
+    q and do are ``[B, H, Nq, d]``, k and v ``[B, H, Nk, d]``. Returns a dict
+    with ``dq`` ([B,H,nq,d]), ``dk``/``dv`` ([B,H,nk,d]), and ``lse``/``D``
+    ([B,H,Nq], the row statistics the oracle computed itself).
     ``qrows``/``kcols`` restrict dq / dk,dv to those rows.
     """
     q, k, v, do = _f64(q, "q"), _f64(k, "k"), _f64(v, "v"), _f64(do, "do")
-    B, H, N, d = q.shape
-    if any(t.shape != q.shape for t in (k, v, do)):
-        raise ValueError("q, k, v, do must share one shape")
+    B, H, Nq, Nk, d = _shapes(q, (k, v), (do,))
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
-    m = _mask(block_mask, N, mask_tile)
+    m = _mask(block_mask, Nq, Nk, mask_tile)
     # a non-NULL index array with count 0 tells the C side to skip that part
-    qr = _idx(qrows, N) if want_dq else np.zeros(1, np.int32)
-    kc = _idx(kcols, N) if want_dkv else np.zeros(1, np.int32)
-    nq = N if qr is None else (qr.size if want_dq else 0)
-    nk = N if kc is None else (kc.size if want_dkv else 0)
+    qr = _idx(qrows, Nq) if want_dq else np.zeros(1, np.int32)
+    kc = _idx(kcols, Nk) if want_dkv else np.zeros(1, np.int32)
+    nq = Nq if qr is None else (qr.size if want_dq else 0)
+    nk = Nk if kc is None else (kc.size if want_dkv else 0)
     dq = np.empty((B, H, nq, d), np.float64)
     dk = np.empty((B, H, nk, d), np.float64)
     dv = np.empty((B, H, nk, d), np.float64)
-    lse = np.empty((B, H, N), np.float64)
-    D = np.empty((B, H, N), np.float64)
-    if B * H * N > 0:
+    lse = np.empty((B, H, Nq), np.float64)
+    D = np.empty((B, H, Nq), np.float64)
+    if B * H * Nq > 0:
         rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
-                                     _ptr(dv), _ptr(lse), _ptr(D), B, H, N, d,
+                                     _ptr(dv), _ptr(lse), _ptr(D), B, H, Nq, Nk, d,
                                      int(bool(causal)), scale, _ptr(m, ctypes.c_ubyte),
                                      mask_tile, _ptr(qr, ctypes.c_int), nq,
                                      _ptr(kc, ctypes.c_int), nk, threads or default_threads())

@@ -6,7 +6,8 @@
  * CUDA library and its Python binding) never calls it, and it shares no
  * code, header, table or constant with that path.
  *
- * What it computes (per batch b, head h; all tensors contiguous [B,H,N,d]):
+ * What it computes (per batch b, head h; Q, O, dO, dQ contiguous [B,H,Nq,d],
+ * K, V, dK, dV contiguous [B,H,Nk,d]; Nq query rows i, Nk key rows j):
  *
  *   s_ij  = scale * sum_c Q_ic K_jc                       for j in J(i)
  *   m_i   = max_j s_ij,  l_i = sum_j exp(s_ij - m_i)
@@ -22,8 +23,13 @@
  *
  * J(i), the keys query i may see (the pages only say that causal masking is
  * applied per tile and that a block-sparse variant exists, so this is a
- * reading): key j is visible iff (!causal || j <= i) and, when a block mask
- * is given, mask[(i / tile) * T + (j / tile)] != 0 with T = ceil(N / tile).
+ * reading): key j is visible iff (!causal || j <= i + Nk - Nq) and, when a
+ * block mask is given, mask[(i / tile) * Tk + (j / tile)] != 0 with
+ * Tq = ceil(Nq / tile), Tk = ceil(Nk / tile) and the mask laid out [Tq][Tk].
+ * With Nq = Nk the causal rule is the pages' j <= i. With Nq != Nk the pages
+ * say nothing; the rule aligns the last query with the last key, so the Nq
+ * queries are the last Nq positions of a sequence of Nk keys (queries that
+ * come before every key, i < Nq - Nk, see nothing).
  * A row with no visible key gets O_i = 0 and LSE_i = -inf.
  *
  * The backward pass is not written out on the pages (the aicassindra page,
@@ -61,17 +67,17 @@
 #define ORACLE_ERR_NOMEM 2
 
 typedef struct {
-  int B, H, N, d;
+  int B, H, Nq, Nk, d;
   int causal;
   double scale;
-  const unsigned char *mask; /* [T][T] or NULL */
+  const unsigned char *mask; /* [Tq][Tk] or NULL */
   int tile;                  /* edge of one mask tile, in rows */
-  int T;                     /* number of mask tiles per side */
+  int Tq, Tk;                /* mask tiles along the queries and along the keys */
 } attn_shape;
 
 static int key_visible(const attn_shape *sh, int i, int j) {
-  if (sh->causal && j > i) return 0;
-  if (sh->mask && !sh->mask[(size_t)(i / sh->tile) * (size_t)sh->T + (size_t)(j / sh->tile)])
+  if (sh->causal && (long)j > (long)i + (long)sh->Nk - (long)sh->Nq) return 0;
+  if (sh->mask && !sh->mask[(size_t)(i / sh->tile) * (size_t)sh->Tk + (size_t)(j / sh->tile)])
     return 0;
   return 1;
 }
@@ -147,23 +153,25 @@ static int run_items(item_fn fn, void *ctx, long n_items, int n_threads, size_t 
 }
 
 static int check_shape(const attn_shape *sh) {
-  if (sh->B < 0 || sh->H < 0 || sh->N < 0 || sh->d <= 0) return ORACLE_ERR_ARG;
+  if (sh->B < 0 || sh->H < 0 || sh->Nq < 0 || sh->Nk < 0 || sh->d <= 0) return ORACLE_ERR_ARG;
   if (sh->mask && sh->tile <= 0) return ORACLE_ERR_ARG;
   return ORACLE_OK;
 }
 
-static attn_shape make_shape(int B, int H, int N, int d, int causal, double scale,
+static attn_shape make_shape(int B, int H, int Nq, int Nk, int d, int causal, double scale,
                              const unsigned char *mask, int tile) {
   attn_shape sh;
   sh.B = B;
   sh.H = H;
-  sh.N = N;
+  sh.Nq = Nq;
+  sh.Nk = Nk;
   sh.d = d;
   sh.causal = causal;
   sh.scale = scale;
   sh.mask = mask;
   sh.tile = tile > 0 ? tile : 1;
-  sh.T = (N + sh.tile - 1) / sh.tile;
+  sh.Tq = (Nq + sh.tile - 1) / sh.tile;
+  sh.Tk = (Nk + sh.tile - 1) / sh.tile;
   return sh;
 }
 
@@ -182,9 +190,9 @@ typedef struct {
  * vis[j] flags; returns the row max (or -inf when no key is visible). */
 static double score_row(const attn_shape *sh, const double *Qh, const double *Kh, int i,
                         double *s, unsigned char *vis) {
-  const int N = sh->N, d = sh->d;
+  const int Nk = sh->Nk, d = sh->d;
   double m = -INFINITY;
-  for (int j = 0; j < N; ++j) {
+  for (int j = 0; j < Nk; ++j) {
     vis[j] = (unsigned char)key_visible(sh, i, j);
     if (!vis[j]) continue;
     s[j] = sh->scale * dot(Qh + (size_t)i * d, Kh + (size_t)j * d, d);
@@ -196,14 +204,15 @@ static double score_row(const attn_shape *sh, const double *Qh, const double *Kh
 static void fwd_item(void *p, long item, double *scratch) {
   fwd_ctx *c = (fwd_ctx *)p;
   const attn_shape *sh = &c->sh;
-  const int N = sh->N, d = sh->d;
+  const int Nk = sh->Nk, d = sh->d;
   const long bh = item / c->n_rows;
   const int r = (int)(item % c->n_rows);
   const int i = c->rows ? c->rows[r] : r;
-  const size_t head = (size_t)bh * (size_t)N * (size_t)d;
-  const double *Qh = c->Q + head, *Kh = c->K + head, *Vh = c->V + head;
+  const double *Qh = c->Q + (size_t)bh * (size_t)sh->Nq * (size_t)d;
+  const double *Kh = c->K + (size_t)bh * (size_t)Nk * (size_t)d;
+  const double *Vh = c->V + (size_t)bh * (size_t)Nk * (size_t)d;
   double *s = scratch;
-  unsigned char *vis = (unsigned char *)(scratch + N);
+  unsigned char *vis = (unsigned char *)(scratch + Nk);
   double *o = c->O + ((size_t)bh * (size_t)c->n_rows + (size_t)r) * (size_t)d;
   double *lse = c->LSE + (size_t)bh * (size_t)c->n_rows + (size_t)r;
 
@@ -214,9 +223,9 @@ static void fwd_item(void *p, long item, double *scratch) {
     return;
   }
   double l = 0.0;
-  for (int j = 0; j < N; ++j)
+  for (int j = 0; j < Nk; ++j)
     if (vis[j]) l += exp(s[j] - m);
-  for (int j = 0; j < N; ++j) {
+  for (int j = 0; j < Nk; ++j) {
     if (!vis[j]) continue;
     const double pij = exp(s[j] - m) / l;
     const double *vj = Vh + (size_t)j * d;
@@ -225,14 +234,14 @@ static void fwd_item(void *p, long item, double *scratch) {
   *lse = m + log(l);
 }
 
-/* O and LSE for the query rows `rows` (all rows when rows == NULL), laid out
- * [B,H,n_rows,d] and [B,H,n_rows]. */
+/* O and LSE for the query rows `rows` (all Nq rows when rows == NULL), laid
+ * out [B,H,n_rows,d] and [B,H,n_rows]. */
 int oracle_forward(const double *Q, const double *K, const double *V, double *O, double *LSE,
-                   int B, int H, int N, int d, int causal, double scale,
+                   int B, int H, int Nq, int Nk, int d, int causal, double scale,
                    const unsigned char *block_mask, int mask_tile, const int *rows, int n_rows,
                    int n_threads) {
   fwd_ctx c;
-  c.sh = make_shape(B, H, N, d, causal, scale, block_mask, mask_tile);
+  c.sh = make_shape(B, H, Nq, Nk, d, causal, scale, block_mask, mask_tile);
   if (check_shape(&c.sh) != ORACLE_OK) return ORACLE_ERR_ARG;
   c.Q = Q;
   c.K = K;
@@ -240,12 +249,13 @@ int oracle_forward(const double *Q, const double *K, const double *V, double *O,
   c.O = O;
   c.LSE = LSE;
   c.rows = rows;
-  c.n_rows = rows ? n_rows : N;
+  c.n_rows = rows ? n_rows : Nq;
   if (rows)
     for (int r = 0; r < n_rows; ++r)
-      if (rows[r] < 0 || rows[r] >= N) return ORACLE_ERR_ARG;
-  /* scratch: s[N] doubles + vis[N] bytes */
-  return run_items(fwd_item, &c, (long)B * H * c.n_rows, n_threads, (size_t)N + (size_t)N / 8 + 2);
+      if (rows[r] < 0 || rows[r] >= Nq) return ORACLE_ERR_ARG;
+  /* scratch: s[Nk] doubles + vis[Nk] bytes */
+  return run_items(fwd_item, &c, (long)B * H * c.n_rows, n_threads,
+                   (size_t)Nk + (size_t)Nk / 8 + 2);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -262,12 +272,13 @@ typedef struct {
 static void tiled_item(void *p, long item, double *scratch) {
   tiled_ctx *c = (tiled_ctx *)p;
   const attn_shape *sh = &c->sh;
-  const int N = sh->N, d = sh->d, bq = c->bq, bk = c->bk;
+  const int Nq = sh->Nq, Nk = sh->Nk, d = sh->d, bq = c->bq, bk = c->bk;
   const long bh = item / c->n_qblocks;
   const int i0 = (int)(item % c->n_qblocks) * bq;
-  const int rows = (i0 + bq <= N) ? bq : N - i0;
-  const size_t head = (size_t)bh * (size_t)N * (size_t)d;
-  const double *Qh = c->Q + head, *Kh = c->K + head, *Vh = c->V + head;
+  const int rows = (i0 + bq <= Nq) ? bq : Nq - i0;
+  const size_t qhead = (size_t)bh * (size_t)Nq * (size_t)d;
+  const size_t khead = (size_t)bh * (size_t)Nk * (size_t)d;
+  const double *Qh = c->Q + qhead, *Kh = c->K + khead, *Vh = c->V + khead;
 
   double *m = scratch;             /* running max        [bq]     */
   double *l = m + bq;              /* running sum        [bq]     */
@@ -280,8 +291,8 @@ static void tiled_item(void *p, long item, double *scratch) {
     l[r] = 0.0;
     for (int x = 0; x < d; ++x) acc[(size_t)r * d + x] = 0.0;
   }
-  for (int j0 = 0; j0 < N; j0 += bk) {
-    const int cols = (j0 + bk <= N) ? bk : N - j0;
+  for (int j0 = 0; j0 < Nk; j0 += bk) {
+    const int cols = (j0 + bk <= Nk) ? bk : Nk - j0;
     for (int r = 0; r < rows; ++r) {
       const int i = i0 + r;
       /* s = (q @ k.T) * scale on this tile, hidden keys held at -inf */
@@ -316,8 +327,8 @@ static void tiled_item(void *p, long item, double *scratch) {
     }
   }
   for (int r = 0; r < rows; ++r) {
-    double *o = c->O + head + (size_t)(i0 + r) * d;
-    double *lse = c->LSE + (size_t)bh * N + (size_t)(i0 + r);
+    double *o = c->O + qhead + (size_t)(i0 + r) * d;
+    double *lse = c->LSE + (size_t)bh * Nq + (size_t)(i0 + r);
     if (l[r] == 0.0) {
       for (int x = 0; x < d; ++x) o[x] = 0.0;
       *lse = -INFINITY;
@@ -329,11 +340,11 @@ static void tiled_item(void *p, long item, double *scratch) {
 }
 
 int oracle_forward_tiled(const double *Q, const double *K, const double *V, double *O,
-                         double *LSE, int B, int H, int N, int d, int causal, double scale,
-                         const unsigned char *block_mask, int mask_tile, int bq, int bk,
-                         int n_threads) {
+                         double *LSE, int B, int H, int Nq, int Nk, int d, int causal,
+                         double scale, const unsigned char *block_mask, int mask_tile, int bq,
+                         int bk, int n_threads) {
   tiled_ctx c;
-  c.sh = make_shape(B, H, N, d, causal, scale, block_mask, mask_tile);
+  c.sh = make_shape(B, H, Nq, Nk, d, causal, scale, block_mask, mask_tile);
   if (check_shape(&c.sh) != ORACLE_OK || bq <= 0 || bk <= 0) return ORACLE_ERR_ARG;
   c.Q = Q;
   c.K = K;
@@ -342,7 +353,7 @@ int oracle_forward_tiled(const double *Q, const double *K, const double *V, doub
   c.LSE = LSE;
   c.bq = bq;
   c.bk = bk;
-  c.n_qblocks = (N + bq - 1) / bq;
+  c.n_qblocks = (Nq + bq - 1) / bq;
   const size_t scratch = (size_t)2 * bq + (size_t)bq * d + (size_t)2 * bq * bk;
   return run_items(tiled_item, &c, (long)B * H * c.n_qblocks, n_threads, scratch);
 }
@@ -354,7 +365,7 @@ typedef struct {
   attn_shape sh;
   const double *Q, *K, *V, *dO;
   double *dQ, *dK, *dV;
-  double *lse_all, *D_all; /* [B*H][N] statistics of every row */
+  double *lse_all, *D_all; /* [B*H][Nq] statistics of every query row */
   const int *qrows;
   int n_q;
   const int *kcols;
@@ -366,16 +377,18 @@ typedef struct {
 static void bwd_row(bwd_ctx *c, long bh, int i, int store_stats, double *dq_out,
                     double *scratch) {
   const attn_shape *sh = &c->sh;
-  const int N = sh->N, d = sh->d;
-  const size_t head = (size_t)bh * (size_t)N * (size_t)d;
-  const double *Qh = c->Q + head, *Kh = c->K + head, *Vh = c->V + head, *dOh = c->dO + head;
-  double *s = scratch;      /* scores, then P           [N] */
-  double *dp = scratch + N; /* dP                        [N] */
-  unsigned char *vis = (unsigned char *)(scratch + 2 * (size_t)N);
+  const int Nq = sh->Nq, Nk = sh->Nk, d = sh->d;
+  const size_t qhead = (size_t)bh * (size_t)Nq * (size_t)d;
+  const size_t khead = (size_t)bh * (size_t)Nk * (size_t)d;
+  const double *Qh = c->Q + qhead, *dOh = c->dO + qhead;
+  const double *Kh = c->K + khead, *Vh = c->V + khead;
+  double *s = scratch;       /* scores, then P           [Nk] */
+  double *dp = scratch + Nk; /* dP                        [Nk] */
+  unsigned char *vis = (unsigned char *)(scratch + 2 * (size_t)Nk);
 
   const double m = score_row(sh, Qh, Kh, i, s, vis);
-  double *lse = c->lse_all + (size_t)bh * N + i;
-  double *Dd = c->D_all + (size_t)bh * N + i;
+  double *lse = c->lse_all + (size_t)bh * Nq + i;
+  double *Dd = c->D_all + (size_t)bh * Nq + i;
   if (m == -INFINITY) {
     if (store_stats) {
       *lse = -INFINITY;
@@ -386,10 +399,10 @@ static void bwd_row(bwd_ctx *c, long bh, int i, int store_stats, double *dq_out,
     return;
   }
   double l = 0.0;
-  for (int j = 0; j < N; ++j)
+  for (int j = 0; j < Nk; ++j)
     if (vis[j]) l += exp(s[j] - m);
   double D = 0.0;
-  for (int j = 0; j < N; ++j) {
+  for (int j = 0; j < Nk; ++j) {
     if (!vis[j]) continue;
     s[j] = exp(s[j] - m) / l;                                          /* P_ij  */
     dp[j] = dot(dOh + (size_t)i * d, Vh + (size_t)j * d, d);           /* dP_ij */
@@ -401,7 +414,7 @@ static void bwd_row(bwd_ctx *c, long bh, int i, int store_stats, double *dq_out,
   }
   if (!dq_out) return;
   for (int x = 0; x < d; ++x) dq_out[x] = 0.0;
-  for (int j = 0; j < N; ++j) {
+  for (int j = 0; j < Nk; ++j) {
     if (!vis[j]) continue;
     const double ds = s[j] * (dp[j] - D);
     const double *kj = Kh + (size_t)j * d;
@@ -412,9 +425,9 @@ static void bwd_row(bwd_ctx *c, long bh, int i, int store_stats, double *dq_out,
 
 static void bwd_stats_item(void *p, long item, double *scratch) {
   bwd_ctx *c = (bwd_ctx *)p;
-  const int N = c->sh.N;
-  const long bh = item / N;
-  const int i = (int)(item % N);
+  const int Nq = c->sh.Nq;
+  const long bh = item / Nq;
+  const int i = (int)(item % Nq);
   bwd_row(c, bh, i, 1, NULL, scratch);
 }
 
@@ -430,12 +443,14 @@ static void bwd_dq_item(void *p, long item, double *scratch) {
 static void bwd_key_item(void *p, long item, double *scratch) {
   bwd_ctx *c = (bwd_ctx *)p;
   const attn_shape *sh = &c->sh;
-  const int N = sh->N, d = sh->d;
+  const int Nq = sh->Nq, Nk = sh->Nk, d = sh->d;
   const long bh = item / c->n_k;
   const int r = (int)(item % c->n_k);
   const int j = c->kcols ? c->kcols[r] : r;
-  const size_t head = (size_t)bh * (size_t)N * (size_t)d;
-  const double *Qh = c->Q + head, *Kh = c->K + head, *Vh = c->V + head, *dOh = c->dO + head;
+  const size_t qhead = (size_t)bh * (size_t)Nq * (size_t)d;
+  const size_t khead = (size_t)bh * (size_t)Nk * (size_t)d;
+  const double *Qh = c->Q + qhead, *dOh = c->dO + qhead;
+  const double *Kh = c->K + khead, *Vh = c->V + khead;
   double *dk = c->dK + ((size_t)bh * c->n_k + r) * (size_t)d;
   double *dv = c->dV + ((size_t)bh * c->n_k + r) * (size_t)d;
   (void)scratch;
@@ -443,10 +458,10 @@ static void bwd_key_item(void *p, long item, double *scratch) {
     dk[x] = 0.0;
     dv[x] = 0.0;
   }
-  for (int i = 0; i < N; ++i) {
+  for (int i = 0; i < Nq; ++i) {
     if (!key_visible(sh, i, j)) continue;
-    const double lse = c->lse_all[(size_t)bh * N + i];
-    const double D = c->D_all[(size_t)bh * N + i];
+    const double lse = c->lse_all[(size_t)bh * Nq + i];
+    const double D = c->D_all[(size_t)bh * Nq + i];
     const double pij = exp(sh->scale * dot(Qh + (size_t)i * d, Kh + (size_t)j * d, d) - lse);
     const double dpij = dot(dOh + (size_t)i * d, Vh + (size_t)j * d, d);
     const double ds = pij * (dpij - D);
@@ -459,17 +474,17 @@ static void bwd_key_item(void *p, long item, double *scratch) {
   for (int x = 0; x < d; ++x) dk[x] *= sh->scale;
 }
 
-/* dQ for the query rows `qrows` ([B,H,n_q,d]; all rows when qrows == NULL),
- * dK and dV for the key rows `kcols` ([B,H,n_k,d]; all when kcols == NULL),
- * and, when lse_out / D_out are given, LSE_i and D_i of every row [B,H,N].
- * Set n_q = 0 (with qrows != NULL) or n_k = 0 to skip that part. */
+/* dQ for the query rows `qrows` ([B,H,n_q,d]; all Nq rows when qrows == NULL),
+ * dK and dV for the key rows `kcols` ([B,H,n_k,d]; all Nk when kcols == NULL),
+ * and, when lse_out / D_out are given, LSE_i and D_i of every query row
+ * [B,H,Nq]. Set n_q = 0 (with qrows != NULL) or n_k = 0 to skip that part. */
 int oracle_backward(const double *Q, const double *K, const double *V, const double *dO,
                     double *dQ, double *dK, double *dV, double *lse_out, double *D_out, int B,
-                    int H, int N, int d, int causal, double scale,
+                    int H, int Nq, int Nk, int d, int causal, double scale,
                     const unsigned char *block_mask, int mask_tile, const int *qrows, int n_q,
                     const int *kcols, int n_k, int n_threads) {
   bwd_ctx c;
-  c.sh = make_shape(B, H, N, d, causal, scale, block_mask, mask_tile);
+  c.sh = make_shape(B, H, Nq, Nk, d, causal, scale, block_mask, mask_tile);
   if (check_shape(&c.sh) != ORACLE_OK) return ORACLE_ERR_ARG;
   c.Q = Q;
   c.K = K;
@@ -479,24 +494,24 @@ int oracle_backward(const double *Q, const double *K, const double *V, const dou
   c.dK = dK;
   c.dV = dV;
   c.qrows = qrows;
-  c.n_q = qrows ? n_q : N;
+  c.n_q = qrows ? n_q : Nq;
   c.kcols = kcols;
-  c.n_k = kcols ? n_k : N;
+  c.n_k = kcols ? n_k : Nk;
   if (qrows)
     for (int r = 0; r < n_q; ++r)
-      if (qrows[r] < 0 || qrows[r] >= N) return ORACLE_ERR_ARG;
+      if (qrows[r] < 0 || qrows[r] >= Nq) return ORACLE_ERR_ARG;
   if (kcols)
     for (int r = 0; r < n_k; ++r)
-      if (kcols[r] < 0 || kcols[r] >= N) return ORACLE_ERR_ARG;
-  const size_t nstat = (size_t)B * H * N;
+      if (kcols[r] < 0 || kcols[r] >= Nk) return ORACLE_ERR_ARG;
+  const size_t nstat = (size_t)B * H * Nq;
   c.lse_all = lse_out ? lse_out : (double *)malloc(sizeof(double) * (nstat + 1));
   c.D_all = D_out ? D_out : (double *)malloc(sizeof(double) * (nstat + 1));
   int rc = ORACLE_OK;
   if (!c.lse_all || !c.D_all) rc = ORACLE_ERR_NOMEM;
-  const size_t row_scratch = 2 * (size_t)N + (size_t)N / 8 + 2;
+  const size_t row_scratch = 2 * (size_t)Nk + (size_t)Nk / 8 + 2;
   /* statistics of every row are needed by the key pass and by the caller */
   if (rc == ORACLE_OK && (c.n_k > 0 || lse_out || D_out))
-    rc = run_items(bwd_stats_item, &c, (long)B * H * N, n_threads, row_scratch);
+    rc = run_items(bwd_stats_item, &c, (long)B * H * Nq, n_threads, row_scratch);
   if (rc == ORACLE_OK && c.n_q > 0)
     rc = run_items(bwd_dq_item, &c, (long)B * H * c.n_q, n_threads, row_scratch);
   if (rc == ORACLE_OK && c.n_k > 0)
