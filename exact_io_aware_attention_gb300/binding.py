@@ -1,8 +1,8 @@
 """Thin Python binding of libfa.so (include/fa.h).
 
-Argument marshalling only: tensors are checked, their device pointers and the
-current CUDA stream are handed to the C ABI, and the status code is turned
-into an exception. Every step of the computation runs in the library's CUDA
+Argument marshalling only: tensors are checked, their device pointers, strides
+and the current CUDA stream are handed to the C ABI, and the status code is
+turned into an exception. Every step of the computation runs in the library's CUDA
 kernels; PyTorch only provides device memory and streams. There is no CPU or
 fallback path: if libfa.so is missing, every call raises.
 """
@@ -22,16 +22,31 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 
+FA_BF16, FA_F32 = 0, 1
+_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
+
+
+class FaTensor(ctypes.Structure):
+    """struct fa_tensor: one [B, H, rows, d] operand with element strides."""
+    _fields_ = [("data", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64), ("stride_n", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 # Every symbol include/fa.h declares, with its ctypes signature.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_tp = ctypes.POINTER(FaTensor)
 SIGNATURES = {
     "fa_abi_version": ([], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_last_error": ([], ctypes.c_char_p),
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_forward_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
+    "fa_forward_ex": ([_tp, _tp, _tp, _tp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
+    "fa_backward_ex": ([_tp] * 5 + [_vp] + [_tp] * 3 +
+                       [_i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "fa_backward_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_backward_noalloc_max_bytes": ([], _sz),
     "fa_device_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i),
@@ -76,7 +91,7 @@ def load_library(path: str | None = None):
 
 def _check(status: int, what: str):
     if status != FA_OK:
-        detail = load_library().fa_last_error().decode() if status == 4 else ""
+        detail = load_library().fa_last_error().decode()
         raise FAError(status, what, detail)
 
 
@@ -88,65 +103,103 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _check_qkv(*ts):
-    q = ts[0]
+def _desc(t, name):
+    """fa_tensor of a [B, H, rows, d] CUDA tensor whose d elements are contiguous."""
+    if not t.is_cuda or t.dim() != 4:
+        raise ValueError(f"{name} must be a 4-D CUDA tensor [B, H, rows, d]")
+    if t.dtype not in _DTYPES:
+        raise ValueError(f"{name}: dtype {t.dtype} is not supported")
+    if t.stride(3) != 1 and t.shape[3] > 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2), _DTYPES[t.dtype], 0)
+
+
+def _shapes(q, kv, qlike=()):
+    """(B, H, Nq, Nk, d) of q [B,H,Nq,d] and k, v [B,H,Nk,d]."""
     if q.dim() != 4:
-        raise ValueError("tensors must be [B, H, N, d]")
-    for t in ts:
-        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("tensors must be contiguous bf16 CUDA tensors")
-        if t.shape != q.shape:
-            raise ValueError("tensors must share one shape")
-    return q.shape
+        raise ValueError("q must be [B, H, Nq, d]")
+    B, H, Nq, d = q.shape
+    Nk = kv[0].shape[2] if kv[0].dim() == 4 else -1
+    for t in kv:
+        if t.dim() != 4 or tuple(t.shape) != (B, H, Nk, d):
+            raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
+    for t in qlike:
+        if tuple(t.shape) != (B, H, Nq, d):
+            raise ValueError("o and do must have q's shape")
+    return B, H, Nq, Nk, d
 
 
-def _mask(block_mask, n):
+def _mask(block_mask, nq, nk):
     if block_mask is None:
         return None
-    t = -(-n // 128)
+    tq, tk = -(-nq // 128), -(-nk // 128)
     if (not block_mask.is_cuda or block_mask.dtype != torch.uint8 or
-            tuple(block_mask.shape) != (t, t) or not block_mask.is_contiguous()):
-        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{t}, {t}]")
+            tuple(block_mask.shape) != (tq, tk) or not block_mask.is_contiguous()):
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{tq}, {tk}]")
     return block_mask
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mask=None,
             out=None, lse=None, o_dtype=torch.bfloat16):
-    """O, LSE = attention(q, k, v): O [B,H,N,d] (bf16, or fp32 with
-    ``o_dtype=torch.float32``), LSE fp32 [B,H,N]."""
-    B, H, N, d = _check_qkv(q, k, v)
+    """O, LSE = attention(q, k, v).
+
+    q is [B, H, Nq, d], k and v [B, H, Nk, d], all bf16 with any strides over
+    the first three dimensions (e.g. permuted views of [B, N, H, d] tensors).
+    O has q's shape and, unless ``out`` is given, q's layout (bf16, or fp32
+    with ``o_dtype=torch.float32``); LSE is fp32 contiguous [B, H, Nq]. With
+    ``causal``, query i sees key j iff j <= i + Nk - Nq.
+    """
+    B, H, Nq, Nk, d = _shapes(q, (k, v))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    mask = _mask(block_mask, N)
+    mask = _mask(block_mask, Nq, Nk)
     if out is None:
-        out = torch.empty((B, H, N, d), dtype=o_dtype, device=q.device)
+        out = torch.empty_like(q, dtype=o_dtype)
     if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fn = load_library().fa_forward_f32 if out.dtype == torch.float32 else load_library().fa_forward
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
-              scale, _ptr(mask), _stream()), "fa_forward")
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (B, H, Nq, d) or tuple(lse.shape) != (B, H, Nq) or \
+            lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("out must be [B, H, Nq, d] and lse contiguous fp32 [B, H, Nq]")
+    dq_, dk_, dv_, do_ = (_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
+    _check(load_library().fa_forward_ex(
+        ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
+        B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), _stream()), "fa_forward_ex")
     return out, lse
 
 
 def backward_workspace_bytes(B, H, N, d) -> int:
+    """Workspace bytes of the backward pass for N query rows per (batch, head)."""
     return int(load_library().fa_backward_workspace_bytes(B, H, N, d))
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
              block_mask=None, workspace=None, dq=None, dk=None, dv=None):
-    """dQ, dK, dV of attention for upstream gradient ``do`` (all bf16 [B,H,N,d])."""
-    B, H, N, d = _check_qkv(q, k, v, o, do)
+    """dQ, dK, dV of attention for upstream gradient ``do``.
+
+    Shapes and layouts as in ``forward``: q, o, do, dq are [B, H, Nq, d], k, v,
+    dk, dv [B, H, Nk, d], all bf16 with any strides over the first three
+    dimensions; each gradient takes its input's layout unless given.
+    """
+    B, H, Nq, Nk, d = _shapes(q, (k, v), (o, do))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    mask = _mask(block_mask, N)
-    nbytes = backward_workspace_bytes(B, H, N, d)
+    mask = _mask(block_mask, Nq, Nk)
+    nbytes = backward_workspace_bytes(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check(load_library().fa_backward(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-        B, H, N, d, int(bool(causal)), scale, _ptr(mask), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream()), "fa_backward")
+    if tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape) or \
+            tuple(dv.shape) != tuple(v.shape):
+        raise ValueError("dq, dk, dv must have the shapes of q, k, v")
+    if tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, Nq]")
+    ds = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"),
+                                   (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    r = [ctypes.byref(x) for x in ds]
+    _check(load_library().fa_backward_ex(
+        r[0], r[1], r[2], r[3], r[4], _ptr(lse), r[5], r[6], r[7], B, H, Nq, Nk, d,
+        int(bool(causal)), scale, _ptr(mask), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream()), "fa_backward_ex")
     return dq, dk, dv
 
 
@@ -187,8 +240,10 @@ class _Attention(torch.autograd.Function):
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = backward(q, k, v, o, do.contiguous(), lse, causal=ctx.causal,
-                              scale=ctx.scale, block_mask=ctx.block_mask)
+        if do.stride(3) != 1:
+            do = do.contiguous()
+        dq, dk, dv = backward(q, k, v, o, do, lse, causal=ctx.causal, scale=ctx.scale,
+                              block_mask=ctx.block_mask)
         return dq, dk, dv, None, None, None
 
 

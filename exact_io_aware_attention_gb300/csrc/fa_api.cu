@@ -61,25 +61,74 @@ cudaError_t status_word(unsigned int **out) {
   return e;
 }
 
-// 2-D bf16 map over [rows][d]: box = 64 columns (128 bytes) x 128 rows, 128-byte swizzle.
-bool encode_rows(CUtensorMap *m, const void *base, long long rows, int d) {
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Element strides of an operand, validated: every stride of a dimension
+// longer than 1 is positive, a multiple of 16 bytes and below 2^40 bytes
+// (the tensor-map limits, which the 16-byte vector loads and stores of the
+// kernels also need); a dimension of length 1 gets a placeholder stride.
+fa_status operand_strides(const fa_tensor *t, int B, int H, int rows, int d, int elem_bytes,
+                          const char *name, fa::RowStrides *out) {
+  if (!t || !t->data) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: null tensor", name);
+    return FA_ERR_INVALID_ARG;
+  }
+  if (t->reserved != 0) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: reserved field is not 0", name);
+    return FA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(t->data)) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: data %p is not 16-byte aligned", name,
+             t->data);
+    return FA_ERR_MISALIGNED;
+  }
+  const long long ext[3] = {B, H, rows};
+  long long st[3] = {t->stride_b, t->stride_h, t->stride_n};
+  const long long unit = 16 / elem_bytes;
+  for (int k = 0; k < 3; ++k) {
+    if (ext[k] <= 1) {
+      st[k] = d;  // never multiplied by a non-zero index
+      continue;
+    }
+    if (st[k] <= 0 || st[k] >= (1LL << 40) / elem_bytes) {
+      snprintf(g_last_error, sizeof(g_last_error), "%s: stride %lld of dimension %d unsupported",
+               name, st[k], k);
+      return FA_ERR_UNSUPPORTED;
+    }
+    if (st[k] % unit != 0) {
+      snprintf(g_last_error, sizeof(g_last_error),
+               "%s: stride %lld of dimension %d is not a multiple of 16 bytes", name, st[k], k);
+      return FA_ERR_MISALIGNED;
+    }
+  }
+  *out = fa::RowStrides{st[0], st[1], st[2]};
+  return FA_OK;
+}
+
+// 4-D bf16 map over [B][H][rows][d] (dims d, rows, H, B): box = 64 columns
+// (128 bytes) x 128 rows x 1 x 1, 128-byte swizzle. A box that runs past
+// `rows` reads zeros there and never the next head.
+bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, int B, int H,
+                    int rows, int d) {
   EncodeTiledFn enc = encoder();
   if (!enc) {
     snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
     return false;
   }
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)fa::kTile};
-  const cuuint32_t elem[2] = {1, 1};
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)st.n_ * 2, (cuuint64_t)st.h_ * 2,
+                                 (cuuint64_t)st.b_ * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)fa::kTile, 1, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
   const CUresult r =
-      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
           elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     snprintf(g_last_error, sizeof(g_last_error),
-             "cuTensorMapEncodeTiled(base=%p, rows=%lld, d=%d) failed: CUresult %d", base, rows, d,
-             (int)r);
+             "cuTensorMapEncodeTiled(base=%p, B=%d, H=%d, rows=%d, d=%d, strides=%lld/%lld/%lld)"
+             " failed: CUresult %d",
+             base, B, H, rows, d, st.b_, st.h_, st.n_, (int)r);
   return r == CUDA_SUCCESS;
 }
 
@@ -92,8 +141,6 @@ int backward_head_group(int bh) {
   const int g = from_env > 0 ? from_env : 8;
   return g < bh ? g : bh;
 }
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Makes the device that owns `ptr` current on the calling thread, which also
 // gives a thread that has not used CUDA yet (e.g. an autograd worker) a
@@ -114,44 +161,71 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Shape checks shared by every entry point; `*empty` is set for a no-op call.
-fa_status check_shape(int B, int H, int N, int d, float scale, bool *empty) {
+fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *empty) {
   *empty = false;
-  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if ((long long)B * H * N == 0) {
+  if ((long long)B * H * Nq == 0) {
     *empty = true;
     return FA_OK;
   }
-  if (N % fa::kTile != 0 || N / fa::kTile > fa::kMaxTiles) return FA_ERR_UNSUPPORTED;
-  if ((long long)B * H * N > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const int n_max = Nq > Nk ? Nq : Nk;
+  if (Nk == 0 || n_max > fa::kTile * fa::kMaxTiles) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H * n_max > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
-fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
-                       int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
-                       void *stream, int o_f32) {
+fa::Shape make_shape(int B, int H, int Nq, int Nk, int d, int causal, const uint8_t *mask) {
+  fa::Shape sh;
+  sh.bh = B * H;
+  sh.heads = H;
+  sh.nq = Nq;
+  sh.nk = Nk;
+  sh.tq = (Nq + fa::kTile - 1) / fa::kTile;
+  sh.tk = (Nk + fa::kTile - 1) / fa::kTile;
+  sh.d = d;
+  sh.causal = causal ? 1 : 0;
+  sh.causal_off = Nk - Nq;
+  sh.mask = mask;
+  return sh;
+}
+
+// The dtype an operand must have: bf16, or fp32 where `f32_ok`.
+fa_status check_dtype(const fa_tensor *t, bool f32_ok, const char *name) {
+  if (t->dtype == FA_BF16 || (f32_ok && t->dtype == FA_F32)) return FA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: dtype %d unsupported", name, (int)t->dtype);
+  return FA_ERR_UNSUPPORTED;
+}
+
+fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                       const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
+                       int causal, float scale, const uint8_t *block_mask, void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, N, d, scale, &empty);
+  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
-    return FA_ERR_MISALIGNED;
-  if ((s = bind_device(Q)) != FA_OK) return s;
   fa::FwdParams p;
   memset(&p, 0, sizeof(p));
-  const long long rows = (long long)B * H * N;
-  if (!encode_rows(&p.tm_q, Q, rows, d) || !encode_rows(&p.tm_k, K, rows, d) ||
-      !encode_rows(&p.tm_v, V, rows, d))
+  fa::RowStrides sq, sk, sv;
+  const int o_bytes = O->dtype == FA_F32 ? 4 : 2;
+  if ((s = check_dtype(Q, false, "Q")) != FA_OK || (s = check_dtype(K, false, "K")) != FA_OK ||
+      (s = check_dtype(V, false, "V")) != FA_OK || (s = check_dtype(O, true, "O")) != FA_OK ||
+      (s = operand_strides(Q, B, H, Nq, d, 2, "Q", &sq)) != FA_OK ||
+      (s = operand_strides(K, B, H, Nk, d, 2, "K", &sk)) != FA_OK ||
+      (s = operand_strides(V, B, H, Nk, d, 2, "V", &sv)) != FA_OK ||
+      (s = operand_strides(O, B, H, Nq, d, o_bytes, "O", &p.so)) != FA_OK)
+    return s;
+  if (!aligned16(LSE)) return FA_ERR_MISALIGNED;
+  if ((s = bind_device(Q->data)) != FA_OK) return s;
+  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d) ||
+      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d) ||
+      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d))
     return FA_ERR_CUDA;
-  p.o = O;
+  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask);
+  p.o = O->data;
   p.lse = LSE;
-  p.mask = block_mask;
-  p.bh = B * H;
-  p.n = N;
-  p.d = d;
-  p.causal = causal ? 1 : 0;
-  p.o_f32 = o_f32;
+  p.o_f32 = O->dtype == FA_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.debug_flags = g_debug_flags.load();
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
@@ -159,6 +233,80 @@ fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, flo
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
   e = fa::launch_forward(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
+}
+
+size_t workspace_bytes(int B, int H, int Nq) {
+  const size_t rows = (size_t)B * H * (size_t)((Nq + fa::kTile - 1) / fa::kTile) * fa::kTile;
+  return 2 * round_up(rows * sizeof(float));
+}
+
+fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                        const fa_tensor *O, const fa_tensor *dO, const float *LSE,
+                        const fa_tensor *dQ, const fa_tensor *dK, const fa_tensor *dV, int B,
+                        int H, int Nq, int Nk, int d, int causal, float scale,
+                        const uint8_t *block_mask, void *workspace, size_t ws_bytes,
+                        void *stream) {
+  bool empty;
+  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (ws_bytes < workspace_bytes(B, H, Nq)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  fa::RowStrides sq, sk, sv;
+  const fa_tensor *all[8] = {Q, K, V, O, dO, dQ, dK, dV};
+  const char *names[8] = {"Q", "K", "V", "O", "dO", "dQ", "dK", "dV"};
+  for (int k = 0; k < 8; ++k)
+    if ((s = check_dtype(all[k], false, names[k])) != FA_OK) return s;
+  if ((s = operand_strides(Q, B, H, Nq, d, 2, "Q", &sq)) != FA_OK ||
+      (s = operand_strides(K, B, H, Nk, d, 2, "K", &sk)) != FA_OK ||
+      (s = operand_strides(V, B, H, Nk, d, 2, "V", &sv)) != FA_OK ||
+      (s = operand_strides(O, B, H, Nq, d, 2, "O", &p.so)) != FA_OK ||
+      (s = operand_strides(dO, B, H, Nq, d, 2, "dO", &p.sdo)) != FA_OK ||
+      (s = operand_strides(dQ, B, H, Nq, d, 2, "dQ", &p.sdq)) != FA_OK ||
+      (s = operand_strides(dK, B, H, Nk, d, 2, "dK", &p.sdk)) != FA_OK ||
+      (s = operand_strides(dV, B, H, Nk, d, 2, "dV", &p.sdv)) != FA_OK)
+    return s;
+  if (!aligned16(LSE) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return FA_ERR_MISALIGNED;
+  if ((s = bind_device(Q->data)) != FA_OK) return s;
+  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d) ||
+      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d) ||
+      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d) ||
+      !encode_operand(&p.tm_do, dO->data, p.sdo, B, H, Nq, d))
+    return FA_ERR_CUDA;
+  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask);
+  p.o = O->data;
+  p.dout = dO->data;
+  p.lse = LSE;
+  const size_t stat_bytes = workspace_bytes(B, H, Nq) / 2;
+  p.delta = static_cast<float *>(workspace);
+  p.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + stat_bytes);
+  p.dq = dQ->data;
+  p.dk = dK->data;
+  p.dv = dV->data;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.head_group = backward_head_group(p.sh.bh);
+  p.debug_flags = g_debug_flags.load();
+  p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
+  cudaError_t e = status_word(&p.status);
+  if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+  e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
+}
+
+// Descriptor of a contiguous [B][H][N][d] tensor.
+fa_tensor contiguous(const void *data, int H, int N, int d, int dtype) {
+  fa_tensor t;
+  t.data = const_cast<void *>(data);
+  t.stride_n = d;
+  t.stride_h = (int64_t)N * d;
+  t.stride_b = (int64_t)H * N * d;
+  t.dtype = dtype;
+  t.reserved = 0;
+  return t;
 }
 
 // ---- measurement hooks ------------------------------------------------------
@@ -281,7 +429,7 @@ fa_status fa_profile_collect(float *total_ms, int *launches, int n) {
 }
 
 
-int fa_abi_version(void) { return 1; }
+int fa_abi_version(void) { return 2; }
 
 const char *fa_status_string(int status) {
   switch (status) {
@@ -298,65 +446,54 @@ const char *fa_status_string(int status) {
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                      int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
                      void *stream) {
-  return forward_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, block_mask, stream, 0);
+  if (!Q || !K || !V || !O) return (long long)B * H * N == 0 ? FA_OK : FA_ERR_INVALID_ARG;
+  const fa_tensor q = contiguous(Q, H, N, d, FA_BF16), k = contiguous(K, H, N, d, FA_BF16),
+                  v = contiguous(V, H, N, d, FA_BF16), o = contiguous(O, H, N, d, FA_BF16);
+  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, stream);
 }
 
 fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, float *LSE,
                          int B, int H, int N, int d, int causal, float scale,
                          const uint8_t *block_mask, void *stream) {
-  return forward_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, block_mask, stream, 1);
+  if (!Q || !K || !V || !O) return (long long)B * H * N == 0 ? FA_OK : FA_ERR_INVALID_ARG;
+  const fa_tensor q = contiguous(Q, H, N, d, FA_BF16), k = contiguous(K, H, N, d, FA_BF16),
+                  v = contiguous(V, H, N, d, FA_BF16), o = contiguous(O, H, N, d, FA_F32);
+  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, stream);
+}
+
+fa_status fa_forward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                        const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
+                        int causal, float scale, const uint8_t *block_mask, void *stream) {
+  return forward_impl(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, block_mask, stream);
 }
 
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return 2 * round_up(rows * sizeof(float));
+  return workspace_bytes(B, H, N);
 }
 
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
                       int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
                       void *workspace, size_t workspace_bytes, void *stream) {
-  bool empty;
-  fa_status s = check_shape(B, H, N, d, scale, &empty);
-  if (s != FA_OK || empty) return s;
-  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
-    return FA_ERR_INVALID_ARG;
-  if (workspace_bytes < fa_backward_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
-      !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) ||
-      (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
-    return FA_ERR_MISALIGNED;
-  if ((s = bind_device(Q)) != FA_OK) return s;
-  fa::BwdParams p;
-  memset(&p, 0, sizeof(p));
-  const long long rows = (long long)B * H * N;
-  if (!encode_rows(&p.tm_q, Q, rows, d) || !encode_rows(&p.tm_k, K, rows, d) ||
-      !encode_rows(&p.tm_v, V, rows, d) || !encode_rows(&p.tm_do, dO, rows, d))
-    return FA_ERR_CUDA;
-  p.o = O;
-  p.dout = dO;
-  p.lse = LSE;
-  const size_t stat_bytes = round_up((size_t)rows * sizeof(float));
-  p.delta = static_cast<float *>(workspace);
-  p.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + stat_bytes);
-  p.dq = dQ;
-  p.dk = dK;
-  p.dv = dV;
-  p.mask = block_mask;
-  p.bh = B * H;
-  p.n = N;
-  p.d = d;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.head_group = backward_head_group(p.bh);
-  p.debug_flags = g_debug_flags.load();
-  p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
-  cudaError_t e = status_word(&p.status);
-  if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
-  e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
+  if (!Q || !K || !V || !O || !dO || !dQ || !dK || !dV)
+    return (long long)B * H * N == 0 ? FA_OK : FA_ERR_INVALID_ARG;
+  const fa_tensor q = contiguous(Q, H, N, d, FA_BF16), k = contiguous(K, H, N, d, FA_BF16),
+                  v = contiguous(V, H, N, d, FA_BF16), o = contiguous(O, H, N, d, FA_BF16),
+                  g = contiguous(dO, H, N, d, FA_BF16), gq = contiguous(dQ, H, N, d, FA_BF16),
+                  gk = contiguous(dK, H, N, d, FA_BF16), gv = contiguous(dV, H, N, d, FA_BF16);
+  return backward_impl(&q, &k, &v, &o, &g, LSE, &gq, &gk, &gv, B, H, N, N, d, causal, scale,
+                       block_mask, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_backward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                         const fa_tensor *O, const fa_tensor *dO, const float *LSE,
+                         const fa_tensor *dQ, const fa_tensor *dK, const fa_tensor *dV, int B,
+                         int H, int Nq, int Nk, int d, int causal, float scale,
+                         const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  return backward_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale,
+                       block_mask, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_device_status(void *stream, unsigned int *code) {
@@ -390,7 +527,7 @@ fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const
                               int B, int H, int N, int d, int causal, float scale,
                               const uint8_t *block_mask, void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, N, d, scale, &empty);
+  fa_status s = check_shape(B, H, N, N, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
   const size_t need = fa_backward_workspace_bytes(B, H, N, d);

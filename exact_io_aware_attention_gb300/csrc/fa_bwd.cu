@@ -14,14 +14,20 @@
 //   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
 //
 // Three kernels on the caller's stream:
-//   fa_bwd_pre        D_i and LSE_i * log2(e)
+//   fa_bwd_pre        D_i and LSE_i * log2(e), padded to whole Q tiles
 //   fa_bwd_dkdv       one CTA per 128-key K/V tile, looping over the Q tiles
-//                     that see it (causal: i >= j; block-sparse: mask[i][j]);
-//                     dK and dV accumulate in tensor memory (this file)
+//                     that see it (causal: a row of the tile sees one of its
+//                     keys; block-sparse: mask[i][j]); dK and dV accumulate in
+//                     tensor memory (this file)
 //   fa_bwd_dq_kernel  one CTA per Q tile, looping over its K/V tiles; dQ
 //                     accumulates in tensor memory (fa_bwd_dq.cu)
 // Each gradient is owned by one CTA, so no cross-CTA reduction is needed;
 // the price is that S and dP are recomputed by both kernels.
+//
+// Rows past the end of a sequence (the last, partial Q or K/V tile) arrive
+// as zeros from the tensor maps. A missing query row has LSE * log2(e) = +inf
+// in the workspace, so its P row is exactly 0 and it adds nothing; a missing
+// key row only feeds its own dK/dV row, which is not stored.
 //
 // fa_bwd_dkdv, 12 warps:
 //   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per step (2 stages)
@@ -81,10 +87,10 @@ struct Bars {
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
 
-// Next Q tile at or after i that sees K/V tile j (T if none).
-__device__ __forceinline__ int next_q(const BwdParams &p, int i, int j, int T) {
-  if (p.mask)
-    while (i < T && p.mask[(size_t)i * T + j] == 0) ++i;
+// Next Q tile at or after i that the block mask lets see K/V tile j (tq if none).
+__device__ __forceinline__ int next_q(const Shape &sh, int i, int j) {
+  if (sh.mask)
+    while (i < sh.tq && sh.mask[(size_t)i * sh.tk + j] == 0) ++i;
   return i;
 }
 
@@ -119,20 +125,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
   const int warp = threadIdx.x >> 5;
-  const int T = p.n / kTile;
+  const Shape &sh = p.sh;
+  const int T = sh.tq;
   // CTAs are ordered head group by head group (p.head_group heads at a
-  // time); within a group the heavy K/V tiles come first (causal: tile j is
-  // seen by T - j Q tiles).
+  // time); within a group the heavy K/V tiles come first (causal: the early
+  // key tiles are seen by the most Q tiles).
   const int hg = p.head_group;
-  const int group = blockIdx.x / (hg * T);
+  const int group = blockIdx.x / (hg * sh.tk);
   const int g_base = group * hg;
-  const int g_size = min(hg, p.bh - g_base);
-  const int g_rank = blockIdx.x - group * hg * T;
+  const int g_size = min(hg, sh.bh - g_base);
+  const int g_rank = blockIdx.x - group * hg * sh.tk;
   const int j = g_rank / g_size;
   const int bh = g_base + g_rank % g_size;
-  const int first = next_q(p, p.causal ? j : 0, j, T);
+  const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
+  const int first = next_q(sh, sh.first_q_tile(j), j);
   const bool any = first < T;
-  const size_t kvrow = (size_t)bh * p.n + (size_t)j * kTile;
+  const size_t stat_head = (size_t)bh * T * kTile;  // this head's rows in the workspace
 
   if (warp == 0 && (threadIdx.x & 31) == 0) {
     mbar_init(bars.kv_full(), 1);
@@ -166,27 +174,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.kv_full(), 2 * L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_2d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, (int)kvrow, bars.kv_full());
-        tma_load_2d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, (int)kvrow, bars.kv_full());
+        tma_load_4d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, j * kTile, h_idx, b_idx,
+                    bars.kv_full());
+        tma_load_4d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, j * kTile, h_idx, b_idx,
+                    bars.kv_full());
       }
       int n = 0;
       bool ok = true;
-      for (int i = first; i < T && ok; i = next_q(p, i + 1, j, T), ++n) {
+      for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
         const int s = n & 1;
         const uint32_t u = n >> 1;
         ok = mbar_wait(bars.q_empty(s), (u & 1u) ^ 1u, st, status_code(kKernBwd, kRoleLoad, 1));
         if (!ok) break;
-        const size_t qrow = (size_t)bh * p.n + (size_t)i * kTile;
         mbar_arrive_expect_tx(bars.q_full(s), 2 * L::kTileBytes + L::kStatBytes);
         for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_2d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, (int)qrow,
-                      bars.q_full(s));
-          tma_load_2d(sdO + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64, (int)qrow,
-                      bars.q_full(s));
+          tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile,
+                      h_idx, b_idx, bars.q_full(s));
+          tma_load_4d(sdO + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile,
+                      h_idx, b_idx, bars.q_full(s));
         }
         const uint32_t sst = s_base + L::kStatOff + s * L::kStatBytes;
-        bulk_load_1d(sst, p.lse2 + qrow, kTile * 4, bars.q_full(s));
-        bulk_load_1d(sst + kTile * 4, p.delta + qrow, kTile * 4, bars.q_full(s));
+        const size_t srow = stat_head + (size_t)i * kTile;
+        bulk_load_1d(sst, p.lse2 + srow, kTile * 4, bars.q_full(s));
+        bulk_load_1d(sst + kTile * 4, p.delta + srow, kTile * 4, bars.q_full(s));
       }
       // teardown: every copy issued has landed
       mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleLoad, 2));
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       int n = 0;
       for (int i = first; i < T && ok; ++n) {
         const int s = n & 1, s1 = s ^ 1;
-        const int inext = next_q(p, i + 1, j, T);
+        const int inext = next_q(sh, i + 1, j);
         ok = mbar_wait(bars.p_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
         if (!ok) break;
         tc_fence_after();
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     const float c = p.scale_log2;
     bool ok = true;
     int n = 0;
-    for (int i = first; i < T && ok; i = next_q(p, i + 1, j, T), ++n) {
+    for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
       const int s = n & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(bars.s_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 1)));
@@ -279,9 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       tc_fence_after();
       const float *lse2 = stat + s * 2 * kTile + 64 * h;
       const float *delta = lse2 + kTile;
-      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); key kr sees query
-      // q only if kr <= q on the diagonal tile of causal attention
-      const bool diag = p.causal && i == j;
+      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); on a tile that
+      // the causal boundary crosses, key kr sees query q only if q >= lo
+      const int lo = (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off)
+                         ? kTile * (j - i) + kr - sh.causal_off
+                         : 0;
       float pr[64];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         for (int x = 0; x < 32; ++x) {
           const int col = 64 * h + 32 * q + x;
           float v = ex2_approx(fmaf(sv[x], c, -lse2[32 * q + x]));
-          pr[32 * q + x] = (diag && col < kr) ? 0.f : v;
+          pr[32 * q + x] = (col < lo) ? 0.f : v;
         }
       }
       // P^T into tensor memory over this warpgroup's first 32 S^T columns
@@ -328,11 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     if (ok && any)
       ok = __all_sync(0xffffffffu, mbar_wait(bars.acc_done(), 0, st,
                                              status_code(kKernBwd, kRoleSoftmax, 6)));
+    // tensor-memory loads are warp-wide; rows past the sequence end store nothing
+    const int krow = j * kTile + kr;  // key row within the head
+    const bool live = krow < sh.nk;
     if (ok) {
       tc_fence_after();
       const uint32_t col = h ? L::kColDK : L::kColDV;
       const float sc = h ? p.scale : 1.f;
-      uint16_t *dst_row = static_cast<uint16_t *>(h ? p.dk : p.dv) + (kvrow + kr) * D;
+      uint16_t *dst_row = static_cast<uint16_t *>(h ? p.dk : p.dv) +
+                          (h ? p.sdk : p.sdv).row(b_idx, h_idx, krow);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         float v[32];
@@ -345,10 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         uint4 *dst = reinterpret_cast<uint4 *>(dst_row + q * 32);
 #pragma unroll
         for (int x = 0; x < 4; ++x)
-          dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
-                              pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
-                              pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
-                              pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
+          if (live)
+            dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
+                                pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
+                                pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
+                                pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
       }
     }
   }
@@ -361,19 +378,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   }
 }
 
-// D_i = dO_i . O_i and LSE_i * log2(e) (0 for a row that sees no key).
+// D_i = dO_i . O_i and LSE_i * log2(e) for every row of every Q tile: a row
+// past the end of the sequence, or one that sees no key (LSE = -inf), gets
+// D = 0 and LSE * log2(e) = +inf, which makes its P row exactly 0.
 // Thread = 8 consecutive elements of a row (16-byte loads).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdParams p) {
   constexpr int kLanesPerRow = D / 8;
-  const size_t rows = (size_t)p.bh * p.n;
+  const Shape &sh = p.sh;
+  const int npad = sh.tq * kTile;
+  const size_t rows = (size_t)sh.bh * npad;
   const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t row = gt / kLanesPerRow;
   const int part = int(gt % kLanesPerRow);
+  const int bh = int(row / npad), n = int(row % npad);
+  const bool live = row < rows && n < sh.nq;
   float acc = 0.f;
-  if (row < rows) {
-    const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.o) + row * D + part * 8);
-    const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) + row * D + part * 8);
+  if (live) {
+    const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
+    const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.o) +
+                                                     p.so.row(b_idx, h_idx, n) + part * 8);
+    const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) +
+                                                     p.sdo.row(b_idx, h_idx, n) + part * 8);
     const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -384,9 +410,10 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) {
-    p.delta[row] = acc;
-    const float l = p.lse[row];
-    p.lse2[row] = isinf(l) ? 0.f : l * 1.4426950408889634f;
+    const float l = live ? p.lse[(size_t)bh * sh.nq + n] : -INFINITY;
+    const bool empty = isinf(l);
+    p.delta[row] = empty ? 0.f : acc;
+    p.lse2[row] = empty ? INFINITY : l * 1.4426950408889634f;
   }
 }
 
@@ -400,7 +427,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const size_t rows = (size_t)p.bh * p.n;
+  const size_t rows = (size_t)p.sh.bh * p.sh.tq * kTile;
   const size_t pre_threads = rows * (D / 8);
   {
     LaunchProbe probe(kKindBwdPre, stream);
@@ -410,7 +437,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   {
     LaunchProbe probe(kKindBwdDkdv, stream);
-    fa_bwd_dkdv<D><<<(p.n / kTile) * p.bh, kThreads, L::kBytes, stream>>>(p);
+    fa_bwd_dkdv<D><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -420,8 +447,8 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
-  if (p.d == 64) return launch_bwd_d<64>(p, stream);
-  if (p.d == 128) return launch_bwd_d<128>(p, stream);
+  if (p.sh.d == 64) return launch_bwd_d<64>(p, stream);
+  if (p.sh.d == 128) return launch_bwd_d<128>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -5,9 +5,11 @@
 // of the definition; the pages leave the backward formulas to a companion
 // article, aicassindra page "The backward pass: recompute instead of
 // store"). One CTA owns a 128-row Q tile and recomputes S and dP for every
-// K/V tile it sees (causal: j <= i; block-sparse: mask[i][j] != 0), so dQ
-// accumulates in tensor memory and is written once, in bf16, without any
-// cross-CTA reduction.
+// K/V tile it sees (causal: a row of the tile sees one of the tile's keys;
+// block-sparse: mask[i][j] != 0), so dQ accumulates in tensor memory and is
+// written once, in bf16, without any cross-CTA reduction. Keys past the end
+// of the sequence (zeros from the tensor map) and keys above the causal
+// boundary get P = 0 on the tiles that need it.
 //
 // 12 warps:
 //   warp 0      TMA producer: Q_i and dO_i once; K_j (3-slot ring), V_j (2 slots)
@@ -96,15 +98,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
 
   // CTA order: head groups of p.head_group heads; heavy Q tiles (late i for
   // causal masking) first within a group.
-  const int T = p.n / kTile;
+  const Shape &sh = p.sh;
+  const int T = sh.tq;
   const int hg = p.head_group;
   const int group = blockIdx.x / (hg * T);
   const int g_base = group * hg;
-  const int g_size = min(hg, p.bh - g_base);
+  const int g_size = min(hg, sh.bh - g_base);
   const int g_rank = blockIdx.x - group * hg * T;
   const int i = T - 1 - g_rank / g_size;
   const int bh = g_base + g_rank % g_size;
-  const int qrow0 = bh * p.n + i * kTile;
+  const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
 
   if (warp == 0 && lane == 0) {
     mbar_init(bars.q_full(), 1);
@@ -133,15 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
   } else if (warp == 2) {
-    // K/V tiles this Q tile sees, ascending
-    const int jmax = p.causal ? i : T - 1;
-    const uint8_t *mrow = p.mask ? p.mask + (size_t)i * T : nullptr;
+    // K/V tiles this Q tile sees, ascending; bit 15: needs element-wise masking
+    const int jmax = sh.last_kv_tile(i);
     int count = 0;
     for (int base = 0; base <= jmax; base += 32) {
       const int j = base + lane;
-      const bool a = j <= jmax && (!mrow || mrow[j] != 0);
+      const bool a = j <= jmax && sh.mask_allows(i, j);
       const uint32_t ball = __ballot_sync(0xffffffffu, a);
-      if (a) list[count + __popc(ball & ((1u << lane) - 1u))] = uint16_t(j);
+      if (a)
+        list[count + __popc(ball & ((1u << lane) - 1u))] =
+            uint16_t(j | (sh.partial(i, j) ? 1u << 15 : 0u));
       count += __popc(ball);
     }
     if (lane == 0) misc[1] = count;
@@ -157,8 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     if (elect_one() && count > 0 && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.q_full(), 2 * L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_2d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0, bars.q_full());
-        tma_load_2d(sdO + c * L::kChunkBytes, &p.tm_do, c * 64, qrow0, bars.q_full());
+        tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
+                    bars.q_full());
+        tma_load_4d(sdO + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx, b_idx,
+                    bars.q_full());
       }
       bool ok = true;
       int nk = 0, nv = 0;  // tiles issued so far
@@ -168,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ok = mbar_wait(bars.k_empty(s), (u & 1u) ^ 1u, st, status_code(kKernBwdDq, kRoleLoad, 1));
         if (!ok) return;
         mbar_arrive_expect_tx(bars.k_full(s), L::kTileBytes);
-        const int row = bh * p.n + list[n] * kTile;
+        const int row = (list[n] & 0x7FFF) * kTile;
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_2d(sK + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_k, c * 64, row,
-                      bars.k_full(s));
+          tma_load_4d(sK + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_k, c * 64, row, h_idx,
+                      b_idx, bars.k_full(s));
         ++nk;
       };
       auto load_v = [&](int n) {
@@ -180,10 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ok = mbar_wait(bars.v_empty(s), (u & 1u) ^ 1u, st, status_code(kKernBwdDq, kRoleLoad, 2));
         if (!ok) return;
         mbar_arrive_expect_tx(bars.v_full(s), L::kTileBytes);
-        const int row = bh * p.n + list[n] * kTile;
+        const int row = (list[n] & 0x7FFF) * kTile;
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_2d(sV + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_v, c * 64, row,
-                      bars.v_full(s));
+          tma_load_4d(sV + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_v, c * 64, row, h_idx,
+                      b_idx, bars.v_full(s));
         ++nv;
       };
       load_k(0);
@@ -281,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     const int r = threadIdx.x & 127;               // query row = TMEM lane
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t t = tmem + lane_off;
-    const size_t grow = (size_t)qrow0 + r;
+    const int qrow = i * kTile + r;                // query row within the head
+    const size_t grow = (size_t)bh * T * kTile + qrow;  // its workspace row
     const float c = p.scale_log2;
     const float lse2 = p.lse2[grow];               // LSE_r * log2(e)
     const float dd = p.delta[grow];                // D_r = dO_r . O_r
@@ -298,15 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         ld_cols32(t + L::kColS + 64 * h + 32, s1);
         tc_fence_before();
         mbar_arrive(bars.s_free());
-        const bool diag = p.causal && list[n] == i;
+        const uint32_t e = list[n];
+        // keys x >= lim of this tile are hidden from this row
+        const int lim = (e >> 15) ? sh.key_limit(i, r, int(e & 0x7FFF)) - 64 * h : 64;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           pr[x] = ex2_approx(fmaf(s0[x], c, -lse2));
           pr[32 + x] = ex2_approx(fmaf(s1[x], c, -lse2));
-          if (diag) {
-            if (64 * h + x > r) pr[x] = 0.f;
-            if (64 * h + 32 + x > r) pr[32 + x] = 0.f;
-          }
+          if (x >= lim) pr[x] = 0.f;
+          if (32 + x >= lim) pr[32 + x] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
@@ -339,10 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     if (ok && count > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_final(), 0, st,
                                              status_code(kKernBwdDq, kRoleSoftmax, 4)));
+    // tensor-memory loads are warp-wide; rows past the sequence end store nothing
+    const bool live = qrow < sh.nq;
     if (ok) {
       tc_fence_after();
       constexpr int kHalf = D / 2;
-      uint16_t *dst_row = static_cast<uint16_t *>(p.dq) + grow * D + h * kHalf;
+      uint16_t *dst_row =
+          static_cast<uint16_t *>(p.dq) + p.sdq.row(b_idx, h_idx, qrow) + h * kHalf;
       const float sc = p.scale;
 #pragma unroll
       for (int q = 0; q < kHalf / 32; ++q) {
@@ -356,10 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         uint4 *dst = reinterpret_cast<uint4 *>(dst_row + 32 * q);
 #pragma unroll
         for (int x = 0; x < 4; ++x)
-          dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
-                              pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
-                              pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
-                              pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
+          if (live)
+            dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
+                                pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
+                                pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
+                                pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
       }
     }
   }
@@ -383,15 +394,15 @@ cudaError_t launch_dq_d(const BwdParams &p, cudaStream_t stream) {
     configured = true;
   }
   LaunchProbe probe(kKindBwdDq, stream);
-  fa_bwd_dq_kernel<D><<<(p.n / kTile) * p.bh, kThreads, L::kBytes, stream>>>(p);
+  fa_bwd_dq_kernel<D><<<p.sh.tq * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream) {
-  if (p.d == 64) return launch_dq_d<64>(p, stream);
-  if (p.d == 128) return launch_dq_d<128>(p, stream);
+  if (p.sh.d == 64) return launch_dq_d<64>(p, stream);
+  if (p.sh.d == 128) return launch_dq_d<128>(p, stream);
   return cudaErrorInvalidValue;
 }
 

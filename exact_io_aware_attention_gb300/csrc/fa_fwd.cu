@@ -9,8 +9,10 @@
 // pass in one loop"): running max m and sum l per row, an unnormalised output
 // accumulator rescaled by exp(m_old - m_new), one division by l at the end.
 // Causal masking is applied per tile (aicassindra page, "Common pitfalls"):
-// tiles above the diagonal are never visited, diagonal tiles are masked
-// element-wise. Block-sparse attention ("Paper Notes: FlashAttention",
+// tiles above the diagonal are never visited, tiles that the diagonal crosses
+// are masked element-wise, and so is the last K/V tile when the key count is
+// not a multiple of 128 (its missing rows arrive as zeros from the tensor
+// map and are hidden). Block-sparse attention ("Paper Notes: FlashAttention",
 // "Experiments & Results") visits only the tiles whose mask byte is set.
 //
 // CTA = one head, two consecutive 128-row Q tiles (t = 0, 1) sharing one
@@ -71,8 +73,10 @@ struct Bars {
   __device__ uint32_t teardown() const { return base + 8 * (6 + 2 * stages); }
 };
 
-// list entry: bits 0-11 key tile j, bit 14 visited by Q tile 0, bit 15 by Q tile 1
+// list entry: bits 0-11 key tile j; bits 12/13: Q tile 0/1 needs element-wise
+// masking on it; bits 14/15: visited by Q tile 0/1
 __device__ __forceinline__ int entry_j(uint32_t e) { return int(e & 0xFFFu); }
+__device__ __forceinline__ bool entry_partial(uint32_t e, int t) { return (e >> (12 + t)) & 1u; }
 __device__ __forceinline__ bool entry_act(uint32_t e, int t) { return (e >> (14 + t)) & 1u; }
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
@@ -95,13 +99,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
 
   // work item: heavy (late) Q-tile pairs first across all heads
-  const int T = p.n / kTile;
-  const int npairs = (T + 1) >> 1;
-  const int bh = blockIdx.x % p.bh;
-  const int pair = npairs - 1 - blockIdx.x / p.bh;
+  const Shape &sh = p.sh;
+  const int npairs = (sh.tq + 1) >> 1;
+  const int bh = blockIdx.x % sh.bh;
+  const int pair = npairs - 1 - blockIdx.x / sh.bh;
   const int i0 = 2 * pair;
-  const bool has1 = (i0 + 1) < T;
-  const int qrow0 = bh * p.n + i0 * kTile;  // first global row of Q tile 0
+  const bool has1 = (i0 + 1) < sh.tq;
+  const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
 
   // ---- setup -------------------------------------------------------------
   if (warp == 0 && lane == 0) {
@@ -127,18 +131,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else if (warp == 2) {
     // K/V tiles visited by either Q tile, ascending, with per-tile flags
     const int i1 = i0 + 1;
-    const int jmax = p.causal ? (has1 ? i1 : i0) : T - 1;
-    const uint8_t *m0 = p.mask ? p.mask + (size_t)i0 * T : nullptr;
-    const uint8_t *m1 = (p.mask && has1) ? p.mask + (size_t)i1 * T : nullptr;
+    const int jmax0 = sh.last_kv_tile(i0);
+    const int jmax1 = has1 ? sh.last_kv_tile(i1) : -1;
+    const int jmax = max(jmax0, jmax1);
     int count = 0;
     for (int base = 0; base <= jmax; base += 32) {
       const int j = base + lane;
-      bool a0 = j <= jmax && (!p.causal || j <= i0) && (!m0 || m0[j] != 0);
-      bool a1 = has1 && j <= jmax && (!m1 || m1[j] != 0);
+      const bool a0 = j <= jmax0 && sh.mask_allows(i0, j);
+      const bool a1 = j <= jmax1 && sh.mask_allows(i1, j);
       const uint32_t ball = __ballot_sync(0xffffffffu, a0 || a1);
       if (a0 || a1) {
         const int slot = count + __popc(ball & ((1u << lane) - 1u));
-        list[slot] = uint16_t(j | (a0 ? 1u << 14 : 0u) | (a1 ? 1u << 15 : 0u));
+        const uint32_t part = (a0 && sh.partial(i0, j) ? 1u << 12 : 0u) |
+                              (a1 && sh.partial(i1, j) ? 1u << 13 : 0u);
+        list[slot] = uint16_t(j | part | (a0 ? 1u << 14 : 0u) | (a1 ? 1u << 15 : 0u));
       }
       count += __popc(ball);
     }
@@ -159,14 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (count > 0) {
         mbar_arrive_expect_tx(bars.q_full(), qbytes);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_2d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0, bars.q_full());
+          tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i0 * kTile, h_idx, b_idx,
+                      bars.q_full());
         if (has1)
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_2d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, qrow0 + kTile,
-                        bars.q_full());
+            tma_load_4d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64,
+                        (i0 + 1) * kTile, h_idx, b_idx, bars.q_full());
       }
       for (int n = 0; n < count && ok; ++n) {
-        const int kvrow = bh * p.n + entry_j(list[n]) * kTile;
+        const int kvrow = entry_j(list[n]) * kTile;
         for (int which = 0; which < 2 && ok; ++which, ++pos) {
           const int s = pos % L::kStages;
           const uint32_t u = pos / L::kStages;
@@ -175,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
           const CUtensorMap *tm = which ? &p.tm_v : &p.tm_k;
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_2d(sKV + s * L::kTileBytes + c * L::kChunkBytes, tm, c * 64, kvrow,
-                        bars.kv_full(s));
+            tma_load_4d(sKV + s * L::kTileBytes + c * L::kChunkBytes, tm, c * 64, kvrow, h_idx,
+                        b_idx, bars.kv_full(s));
         }
       }
       // teardown: wait (bounded) until every copy this thread issued has landed
@@ -302,10 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float s[kTile];
 #pragma unroll
         for (int x = 0; x < kTile; ++x) s[x] = __uint_as_float(sr[x >> 5][x & 31]);
-        if (p.causal && entry_j(e) == qi) {
+        if (entry_partial(e, t)) {  // keys x >= lim are hidden from this row
+          const int lim = sh.key_limit(qi, r, entry_j(e));
 #pragma unroll
           for (int x = 0; x < kTile; ++x)
-            if (x > r) s[x] = -INFINITY;
+            if (x >= lim) s[x] = -INFINITY;
         }
         // row max with 4 independent partial maxima (short dependency chains)
         float mp[4];
@@ -366,9 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (ok && any)
         ok = __all_sync(0xffffffffu, mbar_wait(bars.o_done(), 0, st,
                                                status_code(kKernFwd, kRoleSoftmax, 3)));
+      // tensor-memory loads are warp-wide; rows past the sequence end store nothing
+      const int qrow = qi * kTile + r;  // query row within the head
+      const bool live = qrow < sh.nq;
       if (ok) {
         tc_fence_after();
-        const size_t row = (size_t)(qrow0 + t * kTile + r);
+        // element offset of O's row (indices recomputed here: fewer live registers)
+        const int bh_e = blockIdx.x % sh.bh;
+        const size_t row = p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -380,8 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
             for (int x = 0; x < 32; ++x) o[x] = 0u;
           }
-          if (p.o_f32) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row * D + q * 32);
+          if (!live) {
+          } else if (p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row + q * 32);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
               dst[x] = make_float4(__uint_as_float(o[4 * x]) * inv_l,
@@ -389,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                                    __uint_as_float(o[4 * x + 2]) * inv_l,
                                    __uint_as_float(o[4 * x + 3]) * inv_l);
           } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row * D + q * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row + q * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
               uint4 v;
@@ -402,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
         }
         // LSE = ln(sum_j exp(scale s_ij)) = ln2 * (m + log2 l)
-        p.lse[row] = (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+        if (live)
+          p.lse[(size_t)bh * sh.nq + qrow] =
+            (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -426,8 +442,7 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int T = p.n / kTile;
-  const int grid = ((T + 1) / 2) * p.bh;
+  const int grid = ((p.sh.tq + 1) / 2) * p.sh.bh;
   {
     LaunchProbe probe(kKindFwd, stream);
     fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(p);
@@ -438,8 +453,8 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream) {
-  if (p.d == 64) return launch_fwd_d<64>(p, stream);
-  if (p.d == 128) return launch_fwd_d<128>(p, stream);
+  if (p.sh.d == 64) return launch_fwd_d<64>(p, stream);
+  if (p.sh.d == 128) return launch_fwd_d<128>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -12,12 +12,66 @@ constexpr int kTile = 128;            // rows of a Q tile and keys of a K/V tile
 constexpr int kMaxTiles = 512;        // tiles per sequence the kernels accept (N <= 65536)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit of one kernel-side wait
 
+// Element strides of one [B][H][rows][d] operand: element (b, h, n, c) is at
+// base + b * b_ + h * h_ + n * n_ + c.
+struct RowStrides {
+  long long b_, h_, n_;
+  __host__ __device__ size_t row(int bi, int hi, int n) const {
+    return (size_t)((long long)bi * b_ + (long long)hi * h_ + (long long)n * n_);
+  }
+};
+
+// Shape of one attention problem per (batch, head): nq query rows, nk keys,
+// in tq = ceil(nq/128) Q tiles and tk = ceil(nk/128) K/V tiles. Query i sees
+// key j iff j < nk, (!causal || j <= i + causal_off) and the block mask
+// allows tile (i/128, j/128); causal_off = nk - nq aligns the last query with
+// the last key.
+struct Shape {
+  int bh, heads;                      // B*H and H (bh = b * heads + h)
+  int nq, nk, tq, tk;
+  int d, causal, causal_off;
+  const uint8_t *mask;                // [tq][tk] or null
+
+  // Largest K/V tile with a key visible to some row of Q tile i, or -1.
+  __host__ __device__ int last_kv_tile(int i) const {
+    if (!causal) return tk - 1;
+    const int last_q = min(kTile * i + kTile - 1, nq - 1);
+    const int last_k = last_q + causal_off;             // last visible key of that row
+    if (last_k < 0) return -1;
+    return min(last_k / kTile, tk - 1);
+  }
+  // Smallest Q tile with a row that sees a key of K/V tile j, or tq if none.
+  __host__ __device__ int first_q_tile(int j) const {
+    if (!causal) return 0;
+    const int first_q = kTile * j - causal_off;         // first row that sees key 128 j
+    if (first_q > nq - 1) return tq;
+    return first_q <= 0 ? 0 : first_q / kTile;
+  }
+  // Whether some (query, key) pair of tile (i, j) is hidden by the key count
+  // or by causality, so that the tile needs element-wise masking.
+  __host__ __device__ bool partial(int i, int j) const {
+    if (kTile * j + kTile > nk) return true;
+    return causal && kTile * j + kTile - 1 > kTile * i + causal_off;
+  }
+  // Keys x < key_limit(i, r, j) of K/V tile j are visible to row r of Q tile i.
+  __host__ __device__ int key_limit(int i, int r, int j) const {
+    int lim = nk - kTile * j;
+    if (causal) lim = min(lim, kTile * (i - j) + r + causal_off + 1);
+    return lim;
+  }
+  __host__ __device__ bool mask_allows(int i, int j) const {
+    return !mask || mask[(size_t)i * tk + j] != 0;
+  }
+};
+
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v;       // 2-D bf16 maps [B*H*N rows][d], box 64 x 128, 128B swizzle
-  void *o;                            // bf16 or fp32 [B*H*N][d]
-  float *lse;                         // [B*H*N]
-  const uint8_t *mask;                // [T][T] or null
-  int bh, n, d, causal;
+  // 4-D bf16 maps over [B][H][rows][d] (dims d, rows, H, B), box 64 x 128 x 1 x 1,
+  // 128-byte swizzle; rows past the end of a head read zeros
+  CUtensorMap tm_q, tm_k, tm_v;
+  Shape sh;
+  void *o;                            // bf16 or fp32 rows, strides so
+  RowStrides so;
+  float *lse;                         // [B*H][nq]
   int o_f32;                          // 1: O stored as fp32
   float scale_log2;                   // scale * log2(e)
   unsigned int *status;               // device status word
@@ -27,13 +81,14 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
-  const void *o, *dout;               // bf16 [B*H*N][d]
-  const float *lse;                   // [B*H*N]
-  float *delta;                       // workspace: D_i [B*H*N]
-  float *lse2;                        // workspace: LSE_i * log2(e) [B*H*N]
-  void *dq, *dk, *dv;                 // bf16 outputs
-  const uint8_t *mask;
-  int bh, n, d, causal;
+  Shape sh;
+  const void *o, *dout;               // bf16 rows, strides so / sdo
+  RowStrides so, sdo;
+  const float *lse;                   // [B*H][nq]
+  float *delta;                       // workspace: D_i, [B*H][tq*128]
+  float *lse2;                        // workspace: LSE_i * log2(e), [B*H][tq*128]
+  void *dq, *dk, *dv;                 // bf16 outputs, strides sdq / sdk / sdv
+  RowStrides sdq, sdk, sdv;
   int head_group;                     // CTA order: heads per group (1..bh)
   float scale, scale_log2;
   unsigned int *status;

@@ -10,7 +10,10 @@ Recipe:
   * seed = 1000 * case + tensor index, with Q = 0, K = 1, V = 2, dO = 3,
     mask = 4 (``case`` numbers the workloads listed in ``WORKLOADS``).
   * block mask: ``T x T`` uint8 with T = N / 128, every diagonal tile kept and
-    each off-diagonal tile kept independently with probability ``density``.
+    each off-diagonal tile kept independently with probability ``density``
+    (``Tq x Tk`` for queries and keys of different lengths).
+  * queries and keys of different lengths: Q and dO have Nq rows, K and V Nk
+    rows, drawn with the same seeds.
 """
 from __future__ import annotations
 
@@ -62,21 +65,25 @@ def normal_bf16(shape, seed: int) -> torch.Tensor:
     return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
 
 
-def block_mask(n_tiles: int, density: float, seed: int) -> torch.Tensor:
-    """uint8 [n_tiles, n_tiles]: diagonal kept, off-diagonal kept iid with p=density."""
+def block_mask(n_tiles: int, density: float, seed: int, n_key_tiles: int | None = None):
+    """uint8 [n_tiles, n_key_tiles] (square by default): diagonal kept,
+    off-diagonal kept iid with p=density."""
+    tk = n_tiles if n_key_tiles is None else n_key_tiles
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    keep = torch.rand((n_tiles, n_tiles), generator=g, dtype=torch.float64) < density
-    keep |= torch.eye(n_tiles, dtype=torch.bool)
+    keep = torch.rand((n_tiles, tk), generator=g, dtype=torch.float64) < density
+    keep |= torch.eye(n_tiles, tk, dtype=torch.bool)
     return keep.to(torch.uint8)
 
 
-def make_inputs(B, H, N, d, case: int, with_do: bool = True):
-    """CPU bf16 tensors q, k, v (and do) of shape [B, H, N, d]."""
-    shape = (B, H, N, d)
-    out = {t: normal_bf16(shape, seed_for(case, t)) for t in ("q", "k", "v")}
+def make_inputs(B, H, N, d, case: int, with_do: bool = True, Nk: int | None = None):
+    """CPU bf16 tensors q (and do) of shape [B, H, N, d], k and v of shape
+    [B, H, Nk, d] (Nk = N by default)."""
+    nk = N if Nk is None else Nk
+    out = {t: normal_bf16((B, H, N if t in ("q", "do") else nk, d), seed_for(case, t))
+           for t in ("q", "k", "v")}
     if with_do:
-        out["do"] = normal_bf16(shape, seed_for(case, "do"))
+        out["do"] = normal_bf16((B, H, N, d), seed_for(case, "do"))
     return out
 
 

@@ -17,25 +17,37 @@
  * page, section "The backward pass: recompute instead of store").
  *
  * Conventions shared by every entry point
- *  - Tensors are contiguous row-major [B][H][N][d]; Q, K, V, O, dO, dQ, dK, dV
- *    hold bf16 values (raw 16-bit storage, passed as void*); LSE is fp32
- *    [B][H][N], the natural-log log-sum-exp of the scaled scores of each row.
+ *  - Each batch b and head h has Nq query rows (Q, O, dO, dQ: [Nq][d]) and
+ *    Nk key rows (K, V, dK, dV: [Nk][d]). The plain entry points take
+ *    contiguous row-major [B][H][N][d] tensors with Nq = Nk = N; the _ex entry
+ *    points take an fa_tensor descriptor per operand (any strides over b, h
+ *    and the row, e.g. the [B][N][H][d] layout) and separate Nq and Nk.
+ *    Q, K, V, dO, dQ, dK, dV hold bf16 values (raw 16-bit storage); O is bf16
+ *    (fp32 through fa_forward_f32 or an FA_F32 descriptor). LSE is fp32
+ *    contiguous [B][H][Nq], the natural-log log-sum-exp of the scaled scores
+ *    of each query row.
  *  - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
  *    caller. The library never allocates, frees or synchronises; all work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *    default stream), which must belong to the device that holds Q. Each call
- *    makes that device current on the calling thread. Inputs are only read.
- *  - Supported: d in {64, 128}; N a positive multiple of 128; B, H >= 1;
- *    B*H*N <= 2^31 - 1; scale finite and > 0. B*H*N == 0 is a no-op that
- *    returns FA_OK.
- *  - causal != 0: query i sees key j iff j <= i (0-based, equal lengths).
+ *    makes that device current on the calling thread. Inputs are only read;
+ *    outputs must not overlap one another or an input.
+ *  - Supported: d in {64, 128}; 1 <= Nq, Nk <= 65536 (any length: a last,
+ *    partial tile of 128 rows is handled inside the kernels); B, H >= 1;
+ *    B*H*max(Nq, Nk) <= 2^31 - 1; scale finite and > 0. B*H*Nq == 0 is a
+ *    no-op that returns FA_OK; Nk == 0 with Nq > 0 is FA_ERR_UNSUPPORTED.
+ *  - causal != 0: query i sees key j iff j <= i + Nk - Nq (0-based): with
+ *    Nq = Nk this is the pages' j <= i; with Nq != Nk the last query is
+ *    aligned with the last key, so the queries are the last Nq positions of a
+ *    sequence of Nk keys (this library's reading; the pages treat one
+ *    sequence only). Queries with i < Nq - Nk see no key.
  *  - block_mask: NULL for dense attention, else a DEVICE uint8 array
- *    [T][T], T = N/128, shared by every (b, h); tile (i/128, j/128) is kept
- *    iff its byte is non-zero. With causal also set, both must allow a key.
- *    The pages name a block-sparse variant only ("Paper Notes:
- *    FlashAttention", section "Experiments & Results"); this tile semantics
- *    is this library's reading. A query row that sees no key gets O = 0 and
- *    LSE = -inf.
+ *    [Tq][Tk], Tq = ceil(Nq/128), Tk = ceil(Nk/128), shared by every (b, h);
+ *    tile (i/128, j/128) is kept iff its byte is non-zero. With causal also
+ *    set, both must allow a key. The pages name a block-sparse variant only
+ *    ("Paper Notes: FlashAttention", section "Experiments & Results"); this
+ *    tile semantics is this library's reading. A query row that sees no key
+ *    gets O = 0 and LSE = -inf, and its rows of dQ are 0.
  *  - Host-detectable errors return at once, before anything is enqueued. A
  *    failed launch returns FA_ERR_CUDA. Kernel-side bounded waits that give up
  *    record FA_ERR_TIMEOUT in a device status word that fa_device_status()
@@ -51,11 +63,34 @@
 extern "C" {
 #endif
 
+/* Element types of an fa_tensor. */
+typedef enum fa_dtype {
+  FA_BF16 = 0, /* bfloat16, raw 16-bit storage */
+  FA_F32 = 1   /* IEEE fp32 (accepted for O only) */
+} fa_dtype;
+
+/*
+ * One operand of logical shape [B][H][rows][d]: element (b, h, n, c) is at
+ * data + b*stride_b + h*stride_h + n*stride_n + c (strides in ELEMENTS; the
+ * d elements of a row are contiguous). `data` is a device pointer, 16-byte
+ * aligned. Every stride of a dimension longer than 1 must be positive, a
+ * multiple of 16 bytes (8 bf16 or 4 fp32 elements) and below 2^40 bytes;
+ * strides of dimensions of length 1 are ignored. `reserved` must be 0.
+ */
+typedef struct fa_tensor {
+  void *data;
+  int64_t stride_b;
+  int64_t stride_h;
+  int64_t stride_n;
+  int32_t dtype; /* fa_dtype */
+  int32_t reserved;
+} fa_tensor;
+
 typedef enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, host memory */
-  FA_ERR_UNSUPPORTED = 2, /* valid but outside the supported set (d, N) */
-  FA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
+  FA_ERR_UNSUPPORTED = 2, /* valid but outside the supported set (d, N, dtype, stride) */
+  FA_ERR_MISALIGNED = 3,  /* a pointer or a stride is not a multiple of 16 bytes */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
   FA_ERR_TIMEOUT = 5      /* a kernel-side wait gave up (device status word) */
 } fa_status;
@@ -76,8 +111,9 @@ const char *fa_status_string(int status);
 const char *fa_last_error(void);
 
 /*
- * Forward pass. Reads Q, K, V; writes O (bf16 [B,H,N,d]) and LSE
- * (fp32 [B,H,N]). S and P never reach global memory.
+ * Forward pass, contiguous [B,H,N,d] tensors, Nq = Nk = N. Reads Q, K, V;
+ * writes O (bf16 [B,H,N,d]) and LSE (fp32 [B,H,N]). S and P never reach
+ * global memory.
  */
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                      int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
@@ -93,9 +129,21 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
                          const uint8_t *block_mask, void *stream);
 
 /*
- * Bytes of device workspace fa_backward needs: fp32 D [B,H,N] (D_i = dO_i.O_i)
- * and fp32 LSE*log2(e) [B,H,N], each starting on a 256-byte boundary: O(N),
- * 8 bytes per query row. Returns 0 for invalid sizes.
+ * Forward pass on strided operands with Nq query rows and Nk keys per
+ * (batch, head). Q, K, V are FA_BF16; O is FA_BF16 or FA_F32; LSE is fp32
+ * contiguous [B,H,Nq]. Errors as for fa_forward, plus FA_ERR_UNSUPPORTED or
+ * FA_ERR_MISALIGNED for a descriptor outside the rules of fa_tensor
+ * (fa_last_error() names the operand).
+ */
+fa_status fa_forward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                        const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
+                        int causal, float scale, const uint8_t *block_mask, void *stream);
+
+/*
+ * Bytes of device workspace fa_backward and fa_backward_ex need for N query
+ * rows per (batch, head): fp32 D (D_i = dO_i.O_i) and fp32 LSE*log2(e), each
+ * [B,H,ceil(N/128)*128] and starting on a 256-byte boundary: O(N), 8 bytes
+ * per query row. Returns 0 for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
@@ -111,6 +159,20 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
                       int H, int N, int d, int causal, float scale, const uint8_t *block_mask,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass on strided operands with Nq query rows and Nk keys per
+ * (batch, head): Q, O, dO, dQ have Nq rows, K, V, dK, dV have Nk rows, all
+ * FA_BF16; LSE is fp32 contiguous [B,H,Nq] as written by fa_forward_ex with
+ * the same arguments. The workspace holds at least
+ * fa_backward_workspace_bytes(B,H,Nq,d) bytes, 256-byte aligned.
+ */
+fa_status fa_backward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                         const fa_tensor *O, const fa_tensor *dO, const float *LSE,
+                         const fa_tensor *dQ, const fa_tensor *dK, const fa_tensor *dV, int B,
+                         int H, int Nq, int Nk, int d, int causal, float scale,
+                         const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /*
  * Backward pass without a caller-supplied workspace. The pages have no
@@ -168,9 +230,8 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 
 /*
  * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
- * 0 forward, 1 backward preprocess (D_i, LSE*log2 e, zeroed dQ accumulator),
- * 2 backward main, 3 backward dQ conversion; fa_kernel_name() names them
- * ("" for an unknown id).
+ * 0 forward, 1 backward preprocess (D_i and LSE*log2 e), 2 backward dK/dV,
+ * 3 backward dQ; fa_kernel_name() names them ("" for an unknown id).
  *
  * fa_profile_enable(1): from then on every kernel launch is bracketed by two
  * CUDA events recorded on its stream (no synchronisation, no device memory).

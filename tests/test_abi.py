@@ -37,7 +37,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_status_strings(lib):
-    assert lib.fa_abi_version() == 1
+    assert lib.fa_abi_version() == 2
     for code, name in binding.STATUS_NAMES.items():
         assert lib.fa_status_string(code).decode() == name
     assert lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
@@ -48,6 +48,9 @@ def test_workspace_bytes(lib):
     rows = B * H * N
     up = lambda x: (x + 255) // 256 * 256
     assert lib.fa_backward_workspace_bytes(B, H, N, d) == 2 * up(4 * rows)
+    # statistics are padded to whole 128-row query tiles per (batch, head)
+    assert lib.fa_backward_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * 3 * 5 * 256)
+    assert lib.fa_backward_workspace_bytes(1, 1, 1, 128) == 2 * up(4 * 128)
     assert lib.fa_backward_workspace_bytes(-1, 1, 128, 64) == 0
     assert lib.fa_backward_workspace_bytes(1, 1, 0, 64) == 0
 
@@ -66,8 +69,8 @@ def fwd(lib, q=A, k=A, v=A, o=B_, lse=B_, B=1, H=1, N=256, d=64, causal=0, scale
     (dict(B=-1), INVALID), (dict(N=-128), INVALID), (dict(d=0), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(scale=float("nan")), INVALID),
-    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(N=100), UNSUPPORTED),
-    (dict(N=129), UNSUPPORTED), (dict(N=128 * 513), UNSUPPORTED),
+    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(N=65537), UNSUPPORTED),
+    (dict(N=128 * 513), UNSUPPORTED),
     (dict(B=65536, H=256, N=256), UNSUPPORTED),
     (dict(q=M), MISALIGNED), (dict(v=M), MISALIGNED), (dict(lse=M), MISALIGNED),
 ])
@@ -102,3 +105,81 @@ def test_backward_rejects_bad_arguments(lib):
 def test_binding_refuses_to_run_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         binding.load_library(str(tmp_path / "libfa.so"))
+
+
+# -- strided descriptors and separate query / key lengths ---------------------
+
+def desc(ptr=A, sb=None, sh=None, sn=64, dtype=binding.FA_BF16, reserved=0, H=2, N=300, d=64):
+    sh = N * d if sh is None else sh
+    sb = H * N * d if sb is None else sb
+    return binding.FaTensor(ptr.value if ptr is not None else None, sb, sh, sn, dtype, reserved)
+
+
+def fwd_ex(lib, q=None, k=None, v=None, o=None, lse=B_, B=1, H=2, Nq=300, Nk=300, d=64,
+           causal=1):
+    q = q or desc(N=Nq, H=H, d=d, sn=d)
+    k = k or desc(N=Nk, H=H, d=d, sn=d)
+    v = v or desc(N=Nk, H=H, d=d, sn=d)
+    o = o or desc(ptr=B_, N=Nq, H=H, d=d, sn=d)
+    return lib.fa_forward_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o),
+                             lse, B, H, Nq, Nk, d, causal, 0.125, None, None)
+
+
+# statuses that mean "the arguments passed every host check": the call then
+# fails at the device check (fake pointers: no GPU here, or not device memory)
+PASSED_HOST_CHECKS = (INVALID, 4)
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(q=desc(sn=60)), MISALIGNED),                   # row stride 120 bytes
+    (dict(k=desc(sh=300 * 64 + 4)), MISALIGNED),          # head stride not 16-byte aligned
+    (dict(v=desc(sn=-64)), UNSUPPORTED),                  # negative stride
+    (dict(q=desc(sn=0)), UNSUPPORTED),                    # zero stride of a long dimension
+    (dict(q=desc(sn=1 << 40)), UNSUPPORTED),              # beyond the tensor-map range
+    (dict(q=desc(dtype=2)), UNSUPPORTED),                 # an element type the kernels lack
+    (dict(o=desc(ptr=B_, dtype=7)), UNSUPPORTED),
+    (dict(q=desc(reserved=1)), INVALID),
+    (dict(q=desc(ptr=None)), INVALID),
+    (dict(q=desc(ptr=M)), MISALIGNED),
+    (dict(Nk=0), UNSUPPORTED),
+    (dict(Nq=-1), INVALID),
+    (dict(Nk=65537), UNSUPPORTED),
+])
+def test_forward_ex_rejects_bad_descriptors(lib, case, status):
+    assert fwd_ex(lib, **case) == status
+
+
+@pytest.mark.parametrize("case", [
+    dict(),                                                        # contiguous, N = 300
+    dict(Nq=1, Nk=4097),                                           # one query, ragged keys
+    dict(Nq=1000, Nk=129),
+    dict(q=desc(sn=2 * 64, sh=64, sb=300 * 2 * 64)),               # [B, N, H, d] layout
+    dict(o=desc(ptr=B_, dtype=binding.FA_F32, sn=64, sh=300 * 64)),  # fp32 O
+    dict(B=1, q=desc(sb=3)),                                       # stride of a length-1 dim
+])
+def test_forward_ex_accepts_general_shapes(lib, case):
+    assert fwd_ex(lib, **case) in PASSED_HOST_CHECKS
+
+
+def test_forward_ex_empty_queries_is_noop(lib):
+    assert fwd_ex(lib, Nq=0) == OK
+    assert lib.fa_forward_ex(None, None, None, None, None, 1, 1, 0, 128, 64, 0, 0.1, None,
+                             None) == OK
+
+
+def test_backward_ex_checks_every_operand(lib):
+    ws_bytes = lib.fa_backward_workspace_bytes(1, 2, 300, 64)
+    good = [desc() for _ in range(8)]
+    for k in range(8):
+        ds = list(good)
+        ds[k] = desc(sn=12)
+        r = [ctypes.byref(x) for x in ds]
+        st = lib.fa_backward_ex(r[0], r[1], r[2], r[3], r[4], B_, r[5], r[6], r[7], 1, 2, 300,
+                                300, 64, 1, 0.125, None, B_, ws_bytes, None)
+        assert st == MISALIGNED, k
+    r = [ctypes.byref(x) for x in good]
+    assert lib.fa_backward_ex(r[0], r[1], r[2], r[3], r[4], B_, r[5], r[6], r[7], 1, 2, 300, 300,
+                              64, 1, 0.125, None, B_, ws_bytes - 256, None) == INVALID
+    o32 = desc(dtype=binding.FA_F32)
+    assert lib.fa_backward_ex(r[0], r[1], r[2], ctypes.byref(o32), r[4], B_, r[5], r[6], r[7], 1,
+                              2, 300, 300, 64, 1, 0.125, None, B_, ws_bytes, None) == UNSUPPORTED
