@@ -43,6 +43,10 @@ SIGNATURES = {
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_forward_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
     "fa_forward_ex": ([_tp, _tp, _tp, _tp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp], _i),
+    "fa_forward_split_ex": ([_tp, _tp, _tp, _tp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp,
+                             _sz, _vp], _i),
+    "fa_forward_split_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "fa_forward_num_splits": ([_i, _i, _i, _i, _i, _i], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "fa_backward_ex": ([_tp] * 5 + [_vp] + [_tp] * 3 +
@@ -139,8 +143,15 @@ def _mask(block_mask, nq, nk):
     return block_mask
 
 
+def default_num_splits(B, H, Nq, Nk, d, causal, device=None) -> int:
+    """The library's choice of key splits for the forward pass of this shape
+    (1: no split) on ``device`` (default: the current CUDA device)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(load_library().fa_forward_num_splits(B, H, Nq, Nk, d, int(bool(causal))))
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mask=None,
-            out=None, lse=None, o_dtype=torch.bfloat16):
+            out=None, lse=None, o_dtype=torch.bfloat16, num_splits: int | None = None):
     """O, LSE = attention(q, k, v).
 
     q is [B, H, Nq, d], k and v [B, H, Nk, d], all bf16 with any strides over
@@ -148,6 +159,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
     O has q's shape and, unless ``out`` is given, q's layout (bf16, or fp32
     with ``o_dtype=torch.float32``); LSE is fp32 contiguous [B, H, Nq]. With
     ``causal``, query i sees key j iff j <= i + Nk - Nq.
+
+    ``num_splits``: how many CTAs share the keys of one query tile (their
+    partial results are merged by a second kernel). None lets the library
+    choose: 1 unless the query tiles alone would leave SMs idle, as when
+    decoding against a long cache.
     """
     B, H, Nq, Nk, d = _shapes(q, (k, v))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -160,9 +176,21 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
             lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("out must be [B, H, Nq, d] and lse contiguous fp32 [B, H, Nq]")
     dq_, dk_, dv_, do_ = (_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
-    _check(load_library().fa_forward_ex(
+    lib = load_library()
+    if num_splits is None:
+        num_splits = default_num_splits(B, H, Nq, Nk, d, causal, q.device)
+    if num_splits == 1:
+        _check(lib.fa_forward_ex(
+            ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_),
+            _ptr(lse), B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), _stream()),
+            "fa_forward_ex")
+        return out, lse
+    nbytes = int(lib.fa_forward_split_workspace_bytes(B, H, Nq, d, int(num_splits)))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(lib.fa_forward_split_ex(
         ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
-        B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), _stream()), "fa_forward_ex")
+        B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), int(num_splits), _ptr(ws),
+        nbytes, _stream()), "fa_forward_split_ex")
     return out, lse
 
 

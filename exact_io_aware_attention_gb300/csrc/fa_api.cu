@@ -198,13 +198,32 @@ fa_status check_dtype(const fa_tensor *t, bool f32_ok, const char *name) {
   return FA_ERR_UNSUPPORTED;
 }
 
+// Bytes of one part of the split-forward workspace (256-byte aligned parts).
+size_t split_o_bytes(int B, int H, int Nq, int d, int ns) {
+  return round_up((size_t)ns * B * H * Nq * d * sizeof(float));
+}
+size_t split_lse_bytes(int B, int H, int Nq, int ns) {
+  return round_up((size_t)ns * B * H * Nq * sizeof(float));
+}
+
+constexpr int kMaxSplits = 128;
+
 fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
                        const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
-                       int causal, float scale, const uint8_t *block_mask, void *stream) {
+                       int causal, float scale, const uint8_t *block_mask, int n_split,
+                       void *workspace, size_t ws_bytes, void *stream) {
   bool empty;
   fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (n_split < 1) return FA_ERR_INVALID_ARG;
+  if (n_split > kMaxSplits) return FA_ERR_UNSUPPORTED;
+  if (n_split > 1) {
+    if (!workspace) return FA_ERR_INVALID_ARG;
+    if (ws_bytes < split_o_bytes(B, H, Nq, d, n_split) + split_lse_bytes(B, H, Nq, n_split))
+      return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FA_ERR_MISALIGNED;
+  }
   fa::FwdParams p;
   memset(&p, 0, sizeof(p));
   fa::RowStrides sq, sk, sv;
@@ -226,6 +245,12 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   p.o = O->data;
   p.lse = LSE;
   p.o_f32 = O->dtype == FA_F32 ? 1 : 0;
+  p.n_split = n_split;
+  if (n_split > 1) {
+    p.o_part = static_cast<float *>(workspace);
+    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                           split_o_bytes(B, H, Nq, d, n_split));
+  }
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.debug_flags = g_debug_flags.load();
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
@@ -395,6 +420,7 @@ const char *fa_kernel_name(int kind) {
     case fa::kKindBwdPre: return "fa_bwd_pre";
     case fa::kKindBwdDkdv: return "fa_bwd_dkdv";
     case fa::kKindBwdDq: return "fa_bwd_dq";
+    case fa::kKindFwdCombine: return "fa_fwd_combine";
     default: return "";
   }
 }
@@ -449,7 +475,8 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
   if (!Q || !K || !V || !O) return (long long)B * H * N == 0 ? FA_OK : FA_ERR_INVALID_ARG;
   const fa_tensor q = contiguous(Q, H, N, d, FA_BF16), k = contiguous(K, H, N, d, FA_BF16),
                   v = contiguous(V, H, N, d, FA_BF16), o = contiguous(O, H, N, d, FA_BF16);
-  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, stream);
+  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, 1, nullptr,
+                      0, stream);
 }
 
 fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, float *LSE,
@@ -458,13 +485,49 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
   if (!Q || !K || !V || !O) return (long long)B * H * N == 0 ? FA_OK : FA_ERR_INVALID_ARG;
   const fa_tensor q = contiguous(Q, H, N, d, FA_BF16), k = contiguous(K, H, N, d, FA_BF16),
                   v = contiguous(V, H, N, d, FA_BF16), o = contiguous(O, H, N, d, FA_F32);
-  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, stream);
+  return forward_impl(&q, &k, &v, &o, LSE, B, H, N, N, d, causal, scale, block_mask, 1, nullptr,
+                      0, stream);
 }
 
 fa_status fa_forward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
                         const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
                         int causal, float scale, const uint8_t *block_mask, void *stream) {
-  return forward_impl(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, block_mask, stream);
+  return forward_impl(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, block_mask, 1, nullptr, 0,
+                      stream);
+}
+
+int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal) {
+  (void)d;
+  bool empty;
+  if (check_shape(B, H, Nq, Nk, 64, 1.f, &empty) != FA_OK || empty) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 1;
+  const fa::Shape sh = make_shape(B, H, Nq, Nk, 64, causal, nullptr);
+  const long long ctas = (long long)((sh.tq + 1) / 2) * sh.bh;  // one CTA per SM is resident
+  // K/V tiles the pair with the most work visits
+  const int tiles = sh.last_kv_tile(sh.tq - 1) + 1;
+  if (ctas >= sms || tiles < 4) return 1;
+  long long n = sms / ctas;                 // one wave
+  if (n > tiles / 2) n = tiles / 2;         // at least two K/V tiles per split
+  if (n > kMaxSplits) n = kMaxSplits;
+  return n < 1 ? 1 : (int)n;
+}
+
+size_t fa_forward_split_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 0 || H < 0 || Nq < 0 || d <= 0 || num_splits < 1) return 0;
+  if (num_splits == 1) return 0;
+  return split_o_bytes(B, H, Nq, d, num_splits) + split_lse_bytes(B, H, Nq, num_splits);
+}
+
+fa_status fa_forward_split_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                              const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk,
+                              int d, int causal, float scale, const uint8_t *block_mask,
+                              int num_splits, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  return forward_impl(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, block_mask, num_splits,
+                      workspace, workspace_bytes, stream);
 }
 
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {

@@ -27,6 +27,15 @@
 //   P_t (bf16 pairs): the first 64 columns of S_t (d = 128) or [384+64t, +64) (d = 64)
 // The MMA issue order PV_0(n), S_0(n+1), PV_1(n), S_1(n+1) lets the tensor
 // core work on one Q tile while the other tile's softmax runs.
+//
+// Split over the keys (few Q tiles, many keys, e.g. decoding against a long
+// cache): n_split CTAs share one Q-tile pair, each taking a contiguous share
+// of its K/V tile list, and write their normalised partial O and their LSE.
+// fa_fwd_combine then merges the partials with the block-merge rule of "Paper
+// Notes: FlashAttention" ("Tiling: Block-by-Block Softmax": the merged max is
+// the larger max, each block's sum and output are rescaled by exp(m_block -
+// m), and the sums add), written with LSE_s = m_s + ln l_s:
+//   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -81,7 +90,10 @@ __device__ __forceinline__ bool entry_act(uint32_t e, int t) { return (e >> (14 
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 
-template <int D>
+// kSplit: the keys are split over p.n_split CTAs per Q-tile pair and the
+// epilogue writes this split's partial result (a separate instantiation, so
+// the plain forward carries none of it).
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -98,11 +110,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work item: heavy (late) Q-tile pairs first across all heads
+  // work item: heavy (late) Q-tile pairs first across all heads; the splits
+  // of one pair are adjacent, so they run together and share Q in L2
   const Shape &sh = p.sh;
   const int npairs = (sh.tq + 1) >> 1;
-  const int bh = blockIdx.x % sh.bh;
-  const int pair = npairs - 1 - blockIdx.x / sh.bh;
+  const int n_split = kSplit ? p.n_split : 1;
+  const int split = kSplit ? int(blockIdx.x % n_split) : 0;
+  const int cta = kSplit ? int(blockIdx.x / n_split) : int(blockIdx.x);
+  const int bh = cta % sh.bh;
+  const int pair = npairs - 1 - cta / sh.bh;
   const int i0 = 2 * pair;
   const bool has1 = (i0 + 1) < sh.tq;
   const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
@@ -147,6 +163,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         list[slot] = uint16_t(j | part | (a0 ? 1u << 14 : 0u) | (a1 ? 1u << 15 : 0u));
       }
       count += __popc(ball);
+    }
+    if constexpr (kSplit) {
+      // this CTA's share, entries [lo, hi), moves to the front (ascending
+      // chunks: a chunk's writes land below every later source)
+      const int lo = int((long long)count * split / n_split);
+      const int hi = int((long long)count * (split + 1) / n_split);
+      __syncwarp();
+      for (int base = 0; lo > 0 && base < hi - lo; base += 32) {
+        const bool in = base + lane < hi - lo;
+        const uint16_t v = in ? list[lo + base + lane] : uint16_t(0);
+        __syncwarp();
+        if (in) list[base + lane] = v;
+        __syncwarp();
+      }
+      count = hi - lo;
     }
     if (lane == 0) misc[1] = count;
   }
@@ -379,9 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const bool live = qrow < sh.nq;
       if (ok) {
         tc_fence_after();
-        // element offset of O's row (indices recomputed here: fewer live registers)
-        const int bh_e = blockIdx.x % sh.bh;
-        const size_t row = p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
+        // destination of this row (indices recomputed here: fewer live registers):
+        // O itself, or this split's fp32 partial
+        const int bh_e = int((kSplit ? blockIdx.x / p.n_split : blockIdx.x) % sh.bh);
+        constexpr bool to_part = kSplit;
+        const size_t prow = ((size_t)split * sh.bh + bh) * sh.nq + qrow;
+        const size_t row = to_part ? prow * D : p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
+        float *const o32 = to_part ? p.o_part : static_cast<float *>(p.o);
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -394,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int x = 0; x < 32; ++x) o[x] = 0u;
           }
           if (!live) {
-          } else if (p.o_f32) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row + q * 32);
+          } else if (to_part || p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(o32 + row + q * 32);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
               dst[x] = make_float4(__uint_as_float(o[4 * x]) * inv_l,
@@ -417,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         // LSE = ln(sum_j exp(scale s_ij)) = ln2 * (m + log2 l)
         if (live)
-          p.lse[(size_t)bh * sh.nq + qrow] =
-            (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+          (to_part ? p.lse_part[prow] : p.lse[(size_t)bh * sh.nq + qrow]) =
+              (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -432,20 +467,77 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   }
 }
 
+// Merge of the n_split partial results of one query row (see the top of the
+// file): thread = 8 consecutive columns of a row; the row's n_split LSE values
+// are read by each of its D/8 threads (L1 broadcast). HBM-bound:
+// n_split * (4d + 4) bytes read and 2d + 4 (bf16 O) written per row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_combine(const __grid_constant__ FwdParams p) {
+  constexpr int kLanes = D / 8;
+  const Shape &sh = p.sh;
+  const size_t rows = (size_t)sh.bh * sh.nq;
+  const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t row = gt / kLanes;  // bh * nq + n
+  const int part = int(gt % kLanes);
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < p.n_split; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float l = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < p.n_split; ++s) {
+      const float w = expf(p.lse_part[s * rows + row] - m);  // e^(m_s - m) l_s
+      const float4 *src = reinterpret_cast<const float4 *>(p.o_part + (s * rows + row) * D + part * 8);
+      const float4 a = src[0], b = src[1];
+      l += w;
+      acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+      acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+      acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+      acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+    }
+  }
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const int bh = int(row / sh.nq), n = int(row % sh.nq);
+  const size_t dst = p.so.row(bh / sh.heads, bh % sh.heads, n) + part * 8;
+  if (p.o_f32) {
+    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + dst);
+    o[0] = make_float4(acc[0] * inv_l, acc[1] * inv_l, acc[2] * inv_l, acc[3] * inv_l);
+    o[1] = make_float4(acc[4] * inv_l, acc[5] * inv_l, acc[6] * inv_l, acc[7] * inv_l);
+  } else {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + dst) =
+        make_uint4(pack_bf16x2(acc[0] * inv_l, acc[1] * inv_l), pack_bf16x2(acc[2] * inv_l, acc[3] * inv_l),
+                   pack_bf16x2(acc[4] * inv_l, acc[5] * inv_l), pack_bf16x2(acc[6] * inv_l, acc[7] * inv_l));
+  }
+  if (part == 0) p.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   using L = FwdLayout<D>;
   static bool configured = false;  // attribute set once per process (idempotent anyway)
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_fwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = ((p.sh.tq + 1) / 2) * p.sh.bh;
+  const int grid = ((p.sh.tq + 1) / 2) * p.sh.bh * p.n_split;
   {
     LaunchProbe probe(kKindFwd, stream);
-    fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(p);
+    if (p.n_split > 1)
+      fa_fwd_kernel<D, true><<<grid, kThreads, L::kAlloc, stream>>>(p);
+    else
+      fa_fwd_kernel<D, false><<<grid, kThreads, L::kAlloc, stream>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_split == 1) return e;
+  const size_t threads = (size_t)p.sh.bh * p.sh.nq * (D / 8);
+  {
+    LaunchProbe probe(kKindFwdCombine, stream);
+    fa_fwd_combine<D><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

@@ -73,6 +73,11 @@ struct FwdParams {
   RowStrides so;
   float *lse;                         // [B*H][nq]
   int o_f32;                          // 1: O stored as fp32
+  // Split over the keys: n_split CTAs share the K/V tiles of one Q-tile pair
+  // and write partial results, which fa_fwd_combine merges into O and LSE.
+  int n_split;                        // 1: no split (o_part, lse_part unused)
+  float *o_part;                      // [n_split][B*H][nq][d]: O of each split, normalised
+  float *lse_part;                    // [n_split][B*H][nq]: LSE of each split (-inf: no key)
   float scale_log2;                   // scale * log2(e)
   unsigned int *status;               // device status word
   uint32_t debug_flags;               // kDebug* bits (tests of the failure path only)
@@ -98,7 +103,7 @@ struct BwdParams {
 
 // Kernel ids of the measurement hooks (names in fa_kernel_name()).
 enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdDkdv = 2, kKindBwdDq = 3,
-                        kNumKinds = 4 };
+                        kKindFwdCombine = 4, kNumKinds = 5 };
 
 // Brackets one launch with CUDA events when measurement is enabled
 // (fa_profile_enable); a no-op otherwise.
@@ -115,7 +120,7 @@ class LaunchProbe {
 // consumers' bounded waits run out and report through the status word.
 constexpr uint32_t kDebugSkipLoads = 1u;
 
-cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);
+cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);  // + the merge when split
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_bwd_dq.cu
 

@@ -140,6 +140,40 @@ fa_status fa_forward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
                         int causal, float scale, const uint8_t *block_mask, void *stream);
 
 /*
+ * Forward pass with the keys split over several CTAs, for shapes with few
+ * query tiles per (batch, head), e.g. decoding against a long cache, where
+ * the plain forward would leave most SMs idle. Each of the num_splits shares
+ * of a query tile's K/V tiles yields a normalised partial output O_s and its
+ * LSE_s in `workspace`; a second kernel merges them with the block-merge rule
+ * of "Paper Notes: FlashAttention", section "Tiling: Block-by-Block Softmax"
+ * (merged max = larger max; each block's sum and output rescaled by
+ * exp(m_block - m); the sums add), in LSE form:
+ *     LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+ * The result equals fa_forward_ex's up to rounding. Arguments and errors are
+ * those of fa_forward_ex, plus: num_splits in [1, 128] (1: no split, the
+ * workspace is not used; FA_ERR_INVALID_ARG below 1, FA_ERR_UNSUPPORTED
+ * above 128); workspace: a device buffer of at least
+ * fa_forward_split_workspace_bytes(B,H,Nq,d,num_splits) bytes, 256-byte
+ * aligned, clobbered.
+ */
+fa_status fa_forward_split_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
+                              const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk,
+                              int d, int causal, float scale, const uint8_t *block_mask,
+                              int num_splits, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* Workspace bytes of fa_forward_split_ex: fp32 [num_splits][B][H][Nq][d]
+ * partial outputs and fp32 [num_splits][B][H][Nq] partial LSE, each on a
+ * 256-byte boundary (0 for num_splits = 1 or invalid sizes). */
+size_t fa_forward_split_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/* The library's choice of num_splits for this shape on the calling thread's
+ * current device: 1 when the plain forward already gives every SM a CTA (or
+ * on any error), else about SM count / CTAs, with at least two K/V tiles per
+ * split, at most 128. */
+int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal);
+
+/*
  * Bytes of device workspace fa_backward and fa_backward_ex need for N query
  * rows per (batch, head): fp32 D (D_i = dO_i.O_i) and fp32 LSE*log2(e), each
  * [B,H,ceil(N/128)*128] and starting on a 256-byte boundary: O(N), 8 bytes
@@ -231,7 +265,8 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 /*
  * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
  * 0 forward, 1 backward preprocess (D_i and LSE*log2 e), 2 backward dK/dV,
- * 3 backward dQ; fa_kernel_name() names them ("" for an unknown id).
+ * 3 backward dQ, 4 merge of a split forward; fa_kernel_name() names them
+ * ("" for an unknown id).
  *
  * fa_profile_enable(1): from then on every kernel launch is bracketed by two
  * CUDA events recorded on its stream (no synchronisation, no device memory).

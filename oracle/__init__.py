@@ -11,7 +11,8 @@ takes and returns float64 arrays: queries, outputs and their gradients laid out
 ``[B, H, Nq, d]``, keys and values ``[B, H, Nk, d]``, statistics ``[B, H, Nq]``.
 
 What is computed, and which passage of the pages each part follows, is stated
-at the top of ``attn_oracle.c``. Parity status: every entry point is pinned by
+at the top of ``attn_oracle.c``; ``merge`` / ``merge_lse`` (numpy, below) are
+the pages' rule for combining the softmax results of disjoint key blocks. Parity status: every entry point is pinned by
 ``tests/test_oracle_*.py`` (worked examples printed on the pages, closed forms,
 invariants, brute force and finite differences).
 """
@@ -194,3 +195,49 @@ def backward(q, k, v, do, causal=False, scale=None, block_mask=None, mask_tile=1
                                      _ptr(kc, ctypes.c_int), nk, threads or default_threads())
         _check(rc, "oracle_backward")
     return {"dq": dq, "dk": dk, "dv": dv, "lse": lse, "D": D}
+
+
+def merge(o_parts, m_parts, l_parts):
+    """Merge of per-block softmax results over disjoint key blocks, folding the
+    two-block rule of "Paper Notes: FlashAttention", section "Tiling:
+    Block-by-Block Softmax", left to right:
+
+        m = max(m1, m2),  l = e^(m1 - m) l1 + e^(m2 - m) l2,
+
+    with each block's output rescaled by the same factor as its sum:
+    O = (e^(m1 - m) l1 O1 + e^(m2 - m) l2 O2) / l. O_s is block s's normalised
+    output [..., d], m_s and l_s its row max and row sum [...]; a block in which
+    a row sees no key has m_s = -inf, l_s = 0 and contributes nothing.
+    Returns (O, m, l), float64; a row with no key anywhere gets O = 0,
+    m = -inf, l = 0.
+    """
+    o = np.asarray(o_parts[0], np.float64)
+    m = np.asarray(m_parts[0], np.float64)
+    l = np.asarray(l_parts[0], np.float64)
+    acc = o * l[..., None]  # unnormalised output of the blocks merged so far
+    for o2, m2, l2 in zip(o_parts[1:], m_parts[1:], l_parts[1:]):
+        o2 = np.asarray(o2, np.float64)
+        m2 = np.asarray(m2, np.float64)
+        l2 = np.asarray(l2, np.float64)
+        m_new = np.maximum(m, m2)
+        with np.errstate(invalid="ignore"):
+            a1 = np.where(np.isneginf(m), 0.0, np.exp(m - m_new))
+            a2 = np.where(np.isneginf(m2), 0.0, np.exp(m2 - m_new))
+        l = a1 * l + a2 * l2
+        acc = a1[..., None] * acc + (a2 * l2)[..., None] * o2
+        m = m_new
+    with np.errstate(invalid="ignore", divide="ignore"):
+        out = np.where((l > 0)[..., None], acc / np.where(l > 0, l, 1.0)[..., None], 0.0)
+    return out, m, l
+
+
+def merge_lse(o_parts, lse_parts):
+    """``merge`` for blocks summarised by LSE_s = m_s + ln l_s (the form the
+    library stores): each block enters as (O_s, m = LSE_s, l = 1), or
+    (0, -inf, 0) when LSE_s = -inf. Returns (O, LSE)."""
+    lse_parts = [np.asarray(x, np.float64) for x in lse_parts]
+    ls = [np.where(np.isneginf(x), 0.0, 1.0) for x in lse_parts]
+    o, m, l = merge(o_parts, lse_parts, ls)
+    with np.errstate(divide="ignore"):
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return o, lse

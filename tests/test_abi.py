@@ -183,3 +183,42 @@ def test_backward_ex_checks_every_operand(lib):
     o32 = desc(dtype=binding.FA_F32)
     assert lib.fa_backward_ex(r[0], r[1], r[2], ctypes.byref(o32), r[4], B_, r[5], r[6], r[7], 1,
                               2, 300, 300, 64, 1, 0.125, None, B_, ws_bytes, None) == UNSUPPORTED
+
+
+# -- the forward with the keys split over several CTAs ------------------------
+
+def test_split_workspace_bytes(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    assert lib.fa_forward_split_workspace_bytes(2, 8, 1, 128, 9) == \
+        up(9 * 2 * 8 * 1 * 128 * 4) + up(9 * 2 * 8 * 1 * 4)
+    assert lib.fa_forward_split_workspace_bytes(2, 8, 1, 128, 1) == 0
+    assert lib.fa_forward_split_workspace_bytes(2, 8, 1, 128, 0) == 0
+    assert lib.fa_forward_split_workspace_bytes(-1, 8, 1, 128, 4) == 0
+
+
+def test_num_splits_without_a_device_is_one(lib):
+    # no GPU here: the library cannot read the SM count and declines to split
+    assert lib.fa_forward_num_splits(1, 16, 1, 65536, 128, 1) == 1
+    assert lib.fa_forward_num_splits(1, 16, 0, 65536, 128, 1) == 1
+
+
+def split_fwd(lib, ns, ws=B_, ws_bytes=None, Nq=1, Nk=4096, d=128):
+    q = desc(N=Nq, d=d, sn=d)
+    k = desc(N=Nk, d=d, sn=d)
+    o = desc(ptr=B_, N=Nq, d=d, sn=d)
+    if ws_bytes is None:
+        ws_bytes = lib.fa_forward_split_workspace_bytes(1, 2, Nq, d, max(ns, 1))
+    return lib.fa_forward_split_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k),
+                                   ctypes.byref(o), B_, 1, 2, Nq, Nk, d, 1, 0.1, None, ns, ws,
+                                   ws_bytes, None)
+
+
+def test_split_forward_rejects_bad_arguments(lib):
+    assert split_fwd(lib, 0) == INVALID
+    assert split_fwd(lib, -3) == INVALID
+    assert split_fwd(lib, 129) == UNSUPPORTED
+    assert split_fwd(lib, 4, ws=None) == INVALID
+    assert split_fwd(lib, 4, ws_bytes=1024) == INVALID
+    assert split_fwd(lib, 4, ws=ctypes.c_void_p(0x20010)) == MISALIGNED
+    assert split_fwd(lib, 4) in PASSED_HOST_CHECKS
+    assert split_fwd(lib, 1, ws=None, ws_bytes=0) in PASSED_HOST_CHECKS  # no split: no workspace
