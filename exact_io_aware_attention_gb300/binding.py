@@ -22,8 +22,8 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 
-FA_BF16, FA_F32 = 0, 1
-_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
+FA_BF16, FA_F32, FA_F16 = 0, 1, 2
+_DTYPES = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
 
 class FaTensor(ctypes.Structure):
@@ -151,14 +151,15 @@ def default_num_splits(B, H, Nq, Nk, d, causal, device=None) -> int:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mask=None,
-            out=None, lse=None, o_dtype=torch.bfloat16, num_splits: int | None = None):
+            out=None, lse=None, o_dtype=None, num_splits: int | None = None):
     """O, LSE = attention(q, k, v).
 
-    q is [B, H, Nq, d], k and v [B, H, Nk, d], all bf16 with any strides over
-    the first three dimensions (e.g. permuted views of [B, N, H, d] tensors).
-    O has q's shape and, unless ``out`` is given, q's layout (bf16, or fp32
-    with ``o_dtype=torch.float32``); LSE is fp32 contiguous [B, H, Nq]. With
-    ``causal``, query i sees key j iff j <= i + Nk - Nq.
+    q is [B, H, Nq, d], k and v [B, H, Nk, d], all bf16 or all fp16, with any
+    strides over the first three dimensions (e.g. permuted views of
+    [B, N, H, d] tensors); d is 64, 96 or 128. O has q's shape and, unless
+    ``out`` is given, q's layout and dtype (or ``o_dtype=torch.float32``);
+    LSE is fp32 contiguous [B, H, Nq]. With ``causal``, query i sees key j
+    iff j <= i + Nk - Nq.
 
     ``num_splits``: how many CTAs share the keys of one query tile (their
     partial results are merged by a second kernel). None lets the library
@@ -169,7 +170,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     mask = _mask(block_mask, Nq, Nk)
     if out is None:
-        out = torch.empty_like(q, dtype=o_dtype)
+        out = torch.empty_like(q, dtype=q.dtype if o_dtype is None else o_dtype)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if tuple(out.shape) != (B, H, Nq, d) or tuple(lse.shape) != (B, H, Nq) or \
@@ -204,8 +205,9 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     """dQ, dK, dV of attention for upstream gradient ``do``.
 
     Shapes and layouts as in ``forward``: q, o, do, dq are [B, H, Nq, d], k, v,
-    dk, dv [B, H, Nk, d], all bf16 with any strides over the first three
-    dimensions; each gradient takes its input's layout unless given.
+    dk, dv [B, H, Nk, d], all bf16 or all fp16, with any strides over the
+    first three dimensions; each gradient takes its input's layout unless
+    given.
     """
     B, H, Nq, Nk, d = _shapes(q, (k, v), (o, do))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

@@ -105,11 +105,12 @@ fa_status operand_strides(const fa_tensor *t, int B, int H, int rows, int d, int
   return FA_OK;
 }
 
-// 4-D bf16 map over [B][H][rows][d] (dims d, rows, H, B): box = 64 columns
-// (128 bytes) x 128 rows x 1 x 1, 128-byte swizzle. A box that runs past
-// `rows` reads zeros there and never the next head.
+// 4-D map of 16-bit elements (bf16 or f16) over [B][H][rows][d] (dims d, rows,
+// H, B): box = 64 columns (128 bytes) x 128 rows x 1 x 1, 128-byte swizzle. A
+// box that runs past `rows` reads zeros there and never the next head; one
+// that runs past column d (d = 96) reads zeros in the missing columns.
 bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, int B, int H,
-                    int rows, int d) {
+                    int rows, int d, bool f16) {
   EncodeTiledFn enc = encoder();
   if (!enc) {
     snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
@@ -121,7 +122,8 @@ bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, 
   const cuuint32_t box[4] = {64, (cuuint32_t)fa::kTile, 1, 1};
   const cuuint32_t elem[4] = {1, 1, 1, 1};
   const CUresult r =
-      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+      enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+          const_cast<void *>(base), dims, strides, box,
           elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -165,7 +167,7 @@ fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *em
   *empty = false;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H * Nq == 0) {
     *empty = true;
     return FA_OK;
@@ -176,7 +178,8 @@ fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *em
   return FA_OK;
 }
 
-fa::Shape make_shape(int B, int H, int Nq, int Nk, int d, int causal, const uint8_t *mask) {
+fa::Shape make_shape(int B, int H, int Nq, int Nk, int d, int causal, const uint8_t *mask,
+                     bool f16 = false) {
   fa::Shape sh;
   sh.bh = B * H;
   sh.heads = H;
@@ -187,20 +190,36 @@ fa::Shape make_shape(int B, int H, int Nq, int Nk, int d, int causal, const uint
   sh.d = d;
   sh.causal = causal ? 1 : 0;
   sh.causal_off = Nk - Nq;
+  sh.f16 = f16 ? 1 : 0;
   sh.mask = mask;
   return sh;
 }
 
-// The dtype an operand must have: bf16, or fp32 where `f32_ok`.
-fa_status check_dtype(const fa_tensor *t, bool f32_ok, const char *name) {
-  if (t->dtype == FA_BF16 || (f32_ok && t->dtype == FA_F32)) return FA_OK;
-  snprintf(g_last_error, sizeof(g_last_error), "%s: dtype %d unsupported", name, (int)t->dtype);
+// The inputs' element type: Q decides (bf16 or f16) and every other 16-bit
+// operand must match it; O may also be fp32 where `f32_ok`.
+fa_status check_dtype(const fa_tensor *t, int elem, bool f32_ok, const char *name) {
+  if (t->dtype == elem || (f32_ok && t->dtype == FA_F32)) return FA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: dtype %d unsupported with Q of dtype %d",
+           name, (int)t->dtype, elem);
   return FA_ERR_UNSUPPORTED;
 }
 
+fa_status input_dtype(const fa_tensor *Q, int *elem) {
+  if (Q->dtype != FA_BF16 && Q->dtype != FA_F16) {
+    snprintf(g_last_error, sizeof(g_last_error), "Q: dtype %d unsupported (bf16 or f16)",
+             (int)Q->dtype);
+    return FA_ERR_UNSUPPORTED;
+  }
+  *elem = Q->dtype;
+  return FA_OK;
+}
+
+// Columns the kernels hold per row: a head dimension of 96 runs as 128.
+int padded_d(int d) { return d == 96 ? 128 : d; }
+
 // Bytes of one part of the split-forward workspace (256-byte aligned parts).
 size_t split_o_bytes(int B, int H, int Nq, int d, int ns) {
-  return round_up((size_t)ns * B * H * Nq * d * sizeof(float));
+  return round_up((size_t)ns * B * H * Nq * padded_d(d) * sizeof(float));
 }
 size_t split_lse_bytes(int B, int H, int Nq, int ns) {
   return round_up((size_t)ns * B * H * Nq * sizeof(float));
@@ -228,8 +247,10 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   memset(&p, 0, sizeof(p));
   fa::RowStrides sq, sk, sv;
   const int o_bytes = O->dtype == FA_F32 ? 4 : 2;
-  if ((s = check_dtype(Q, false, "Q")) != FA_OK || (s = check_dtype(K, false, "K")) != FA_OK ||
-      (s = check_dtype(V, false, "V")) != FA_OK || (s = check_dtype(O, true, "O")) != FA_OK ||
+  int elem = FA_BF16;
+  if ((s = input_dtype(Q, &elem)) != FA_OK || (s = check_dtype(K, elem, false, "K")) != FA_OK ||
+      (s = check_dtype(V, elem, false, "V")) != FA_OK ||
+      (s = check_dtype(O, elem, true, "O")) != FA_OK ||
       (s = operand_strides(Q, B, H, Nq, d, 2, "Q", &sq)) != FA_OK ||
       (s = operand_strides(K, B, H, Nk, d, 2, "K", &sk)) != FA_OK ||
       (s = operand_strides(V, B, H, Nk, d, 2, "V", &sv)) != FA_OK ||
@@ -237,11 +258,12 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
     return s;
   if (!aligned16(LSE)) return FA_ERR_MISALIGNED;
   if ((s = bind_device(Q->data)) != FA_OK) return s;
-  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d) ||
-      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d) ||
-      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d))
+  const bool f16 = elem == FA_F16;
+  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d, f16) ||
+      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d, f16) ||
+      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d, f16))
     return FA_ERR_CUDA;
-  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask);
+  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask, f16);
   p.o = O->data;
   p.lse = LSE;
   p.o_f32 = O->dtype == FA_F32 ? 1 : 0;
@@ -282,8 +304,10 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   fa::RowStrides sq, sk, sv;
   const fa_tensor *all[8] = {Q, K, V, O, dO, dQ, dK, dV};
   const char *names[8] = {"Q", "K", "V", "O", "dO", "dQ", "dK", "dV"};
-  for (int k = 0; k < 8; ++k)
-    if ((s = check_dtype(all[k], false, names[k])) != FA_OK) return s;
+  int elem = FA_BF16;
+  if ((s = input_dtype(Q, &elem)) != FA_OK) return s;
+  for (int k = 1; k < 8; ++k)
+    if ((s = check_dtype(all[k], elem, false, names[k])) != FA_OK) return s;
   if ((s = operand_strides(Q, B, H, Nq, d, 2, "Q", &sq)) != FA_OK ||
       (s = operand_strides(K, B, H, Nk, d, 2, "K", &sk)) != FA_OK ||
       (s = operand_strides(V, B, H, Nk, d, 2, "V", &sv)) != FA_OK ||
@@ -296,12 +320,13 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   if (!aligned16(LSE) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
     return FA_ERR_MISALIGNED;
   if ((s = bind_device(Q->data)) != FA_OK) return s;
-  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d) ||
-      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d) ||
-      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d) ||
-      !encode_operand(&p.tm_do, dO->data, p.sdo, B, H, Nq, d))
+  const bool f16 = elem == FA_F16;
+  if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d, f16) ||
+      !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d, f16) ||
+      !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d, f16) ||
+      !encode_operand(&p.tm_do, dO->data, p.sdo, B, H, Nq, d, f16))
     return FA_ERR_CUDA;
-  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask);
+  p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask, f16);
   p.o = O->data;
   p.dout = dO->data;
   p.lse = LSE;

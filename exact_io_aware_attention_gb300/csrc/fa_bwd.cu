@@ -35,7 +35,7 @@
 //   warps 4-7   thread = key row: P^T and dS^T for queries 0..63; then dV out
 //   warps 8-11  thread = key row: P^T and dS^T for queries 64..127; then dK out
 // Tensor memory (512 columns): [0,128) S^T, [128,256) dP^T, then dV and dK
-// (d columns each). P^T and dS^T (bf16 pairs) are the tensor-memory A
+// (d columns each). P^T and dS^T (16-bit pairs) are the tensor-memory A
 // operands of dV += P^T dO and dK += dS^T Q: the warpgroup for queries
 // 64h..64h+63 writes them over the first 32 of its own 64 S^T (dP^T)
 // columns once it has read them. Shared memory: K_j, V_j, Q_i[2], dO_i[2],
@@ -106,7 +106,10 @@ __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
 }
 
-template <int D>
+// kF16: f16 elements instead of bf16. D is 64 or 128; a head dimension of 96
+// runs as 128 (the tensor maps read zeros in columns 96..127) and only the
+// first sh.d columns of dK and dV are stored.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant__ BwdParams p) {
   using L = DkdvLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -209,15 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   } else if (warp == 1) {
     // ---- tcgen05 issuer ----------------------------------------------------
     if (elect_one()) {
-      constexpr uint32_t kIdSq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S^T, dP^T
-      constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, 0, 1);     // dV, dK: B MN-major
+      constexpr uint32_t kIdSq = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_f32acc(kTile, D, 0, 1, kF16);     // dV, dK: B MN-major
       bool ok = !any || mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleMma, 1));
       // X^T = A Y^T with A in {K_j, V_j} and Y in {Q_i, dO_i}: K-major over d
       auto issue_sq = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + col, sdesc_sw128(a_base + off, 16, 1024),
+          mma_f16kind_ss(tmem + col, sdesc_sw128(a_base + off, 16, 1024),
                       sdesc_sw128(b_base + off, 16, 1024), kIdSq, kk > 0);
         }
       };
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       auto issue_acc = [&](uint32_t a_col, uint32_t y_base, uint32_t col, bool first) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + col, tmem + a_col + packed_col(kk),
+          mma_f16kind_ts(tmem + col, tmem + a_col + packed_col(kk),
                       sdesc_sw128(y_base + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
                       (!first || kk > 0) ? 1u : 0u);
       };
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(pr[2 * x], pr[2 * x + 1]);
+        for (int x = 0; x < 32; ++x) pk[x] = pack2<kF16>(pr[2 * x], pr[2 * x + 1]);
         tmem_st32(t + L::kColS + 64 * h, pk);
         tmem_wait_st();
       }
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
 #pragma unroll
         for (int x = 0; x < 32; x += 2)
-          dsp[16 * q + x / 2] = pack_bf16x2(pr[32 * q + x] * (dp[x] - delta[32 * q + x]),
+          dsp[16 * q + x / 2] = pack2<kF16>(pr[32 * q + x] * (dp[x] - delta[32 * q + x]),
                                             pr[32 * q + x + 1] * (dp[x + 1] - delta[32 * q + x + 1]));
       }
       tmem_st32(t + L::kColDP + 64 * h, dsp);
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
                           (h ? p.sdk : p.sdv).row(b_idx, h_idx, krow);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
+        if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
         float v[32];
         if (any) {
           ld_cols32(t + col + q * 32, v);
@@ -362,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 #pragma unroll
         for (int x = 0; x < 4; ++x)
           if (live)
-            dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
-                                pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
-                                pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
-                                pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
+            dst[x] = make_uint4(pack2<kF16>(v[8 * x] * sc, v[8 * x + 1] * sc),
+                                pack2<kF16>(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
+                                pack2<kF16>(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
+                                pack2<kF16>(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
       }
     }
   }
@@ -381,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 // D_i = dO_i . O_i and LSE_i * log2(e) for every row of every Q tile: a row
 // past the end of the sequence, or one that sees no key (LSE = -inf), gets
 // D = 0 and LSE * log2(e) = +inf, which makes its P row exactly 0.
-// Thread = 8 consecutive elements of a row (16-byte loads).
-template <int D>
+// Thread = 8 consecutive elements of a row (16-byte loads); with a head
+// dimension of 96 (run as D = 128) the last 4 threads of a row add nothing.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdParams p) {
   constexpr int kLanesPerRow = D / 8;
   const Shape &sh = p.sh;
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
   const size_t row = gt / kLanesPerRow;
   const int part = int(gt % kLanesPerRow);
   const int bh = int(row / npad), n = int(row % npad);
-  const bool live = row < rows && n < sh.nq;
+  const bool live = row < rows && n < sh.nq && part * 8 < sh.d;
   float acc = 0.f;
   if (live) {
     const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
@@ -403,27 +408,30 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
     const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      acc = fmaf(__uint_as_float(ow[h] << 16), __uint_as_float(gw[h] << 16), acc);
-      acc = fmaf(__uint_as_float(ow[h] & 0xffff0000u), __uint_as_float(gw[h] & 0xffff0000u), acc);
+      float o0, o1, g0, g1;
+      unpack2<kF16>(ow[h], o0, o1);
+      unpack2<kF16>(gw[h], g0, g1);
+      acc = fmaf(o0, g0, acc);
+      acc = fmaf(o1, g1, acc);
     }
   }
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) {
     const float l = live ? p.lse[(size_t)bh * sh.nq + n] : -INFINITY;
-    const bool empty = isinf(l);
+    const bool empty = isinf(l);  // also the rows past the end (l = -inf)
     p.delta[row] = empty ? 0.f : acc;
     p.lse2[row] = empty ? INFINITY : l * 1.4426950408889634f;
   }
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   using L = DkdvLayout<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kBytes);
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv<D, kF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -431,13 +439,13 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   const size_t pre_threads = rows * (D / 8);
   {
     LaunchProbe probe(kKindBwdPre, stream);
-    fa_bwd_pre<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, stream>>>(p);
+    fa_bwd_pre<D, kF16><<<(unsigned)((pre_threads + 255) / 256), 256, 0, stream>>>(p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
     LaunchProbe probe(kKindBwdDkdv, stream);
-    fa_bwd_dkdv<D><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
+    fa_bwd_dkdv<D, kF16><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -447,8 +455,10 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
-  if (p.sh.d == 64) return launch_bwd_d<64>(p, stream);
-  if (p.sh.d == 128) return launch_bwd_d<128>(p, stream);
+  const bool f16 = p.sh.f16 != 0;
+  if (p.sh.d == 64) return f16 ? launch_bwd_d<64, true>(p, stream) : launch_bwd_d<64, false>(p, stream);
+  if (p.sh.d == 96 || p.sh.d == 128)
+    return f16 ? launch_bwd_d<128, true>(p, stream) : launch_bwd_d<128, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

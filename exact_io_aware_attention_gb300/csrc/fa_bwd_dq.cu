@@ -7,7 +7,7 @@
 // store"). One CTA owns a 128-row Q tile and recomputes S and dP for every
 // K/V tile it sees (causal: a row of the tile sees one of the tile's keys;
 // block-sparse: mask[i][j] != 0), so dQ accumulates in tensor memory and is
-// written once, in bf16, without any cross-CTA reduction. Keys past the end
+// written once, in 16 bits, without any cross-CTA reduction. Keys past the end
 // of the sequence (zeros from the tensor map) and keys above the causal
 // boundary get P = 0 on the tiles that need it.
 //
@@ -18,7 +18,7 @@
 //   warps 4-7   thread = query row; keys 0..63 of each tile
 //   warps 8-11  thread = query row; keys 64..127 of each tile
 // Tensor memory: [0,128) S_ij, [128,256) dP_ij, [256,320) dS_ij as packed
-// bf16 pairs (the A operand of the dQ MMA), [384,384+d) dQ accumulator.
+// 16-bit pairs (the A operand of the dQ MMA), [384,384+d) dQ accumulator.
 // MMA order per step n: S(n+1) once S(n) has been read, dQ += dS(n) K_n once
 // dS(n) is in tensor memory, then dP(n+1).
 #include <math.h>
@@ -79,7 +79,10 @@ __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
 }
 
-template <int D>
+// kF16: f16 elements instead of bf16. D is 64 or 128; a head dimension of 96
+// runs as 128 (the tensor maps read zeros in columns 96..127) and only the
+// first sh.d columns of dQ are stored.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -212,15 +215,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   } else if (warp == 1) {
     // ---- tcgen05 issuer ----------------------------------------------------
     if (elect_one()) {
-      constexpr uint32_t kIdSq = idesc_bf16_f32(kTile, kTile, 0, 0);  // S, dP: K-major over d
-      constexpr uint32_t kIdDq = idesc_bf16_f32(kTile, D, 0, 1);      // dS (TMEM) x K (MN-major)
+      constexpr uint32_t kIdSq = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // S, dP: K-major over d
+      constexpr uint32_t kIdDq = idesc_f32acc(kTile, D, 0, 1, kF16);      // dS (TMEM) x K (MN-major)
       bool ok = count == 0 || mbar_wait(bars.q_full(), 0, st, status_code(kKernBwdDq, kRoleMma, 1));
       // S = Q K_n^T and dP = dO V_n^T, both operands K-major over d
       auto issue_sq = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + col, sdesc_sw128(a_base + off, 16, 1024),
+          mma_f16kind_ss(tmem + col, sdesc_sw128(a_base + off, 16, 1024),
                       sdesc_sw128(b_base + off, 16, 1024), kIdSq, kk > 0);
         }
       };
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         const uint32_t kb = sK + ks * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + L::kColDQ, tmem + L::kColDS + kk * 8,
+          mma_f16kind_ts(tmem + L::kColDQ, tmem + L::kColDS + kk * 8,
                       sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024), kIdDq,
                       (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bars.dq_step());
@@ -320,14 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                                              status_code(kKernBwdDq, kRoleSoftmax, 2)));
       if (!ok) break;
       tc_fence_after();
-      uint32_t dsp[32];  // dS as packed bf16 pairs: keys (2x, 2x+1) of this half
+      uint32_t dsp[32];  // dS as packed 16-bit pairs: keys (2x, 2x+1) of this half
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         float dp[32];
         ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
 #pragma unroll
         for (int x = 0; x < 32; x += 2)
-          dsp[16 * q + x / 2] = pack_bf16x2(pr[32 * q + x] * (dp[x] - dd),
+          dsp[16 * q + x / 2] = pack2<kF16>(pr[32 * q + x] * (dp[x] - dd),
                                             pr[32 * q + x + 1] * (dp[x + 1] - dd));
       }
       // the dS columns are free once the previous dQ MMA has read them
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       const float sc = p.scale;
 #pragma unroll
       for (int q = 0; q < kHalf / 32; ++q) {
+        if (D == 128 && h * kHalf + q * 32 >= sh.d) break;  // head dimension 96
         float v[32];
         if (count > 0) {
           ld_cols32(t + L::kColDQ + h * kHalf + 32 * q, v);
@@ -367,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
 #pragma unroll
         for (int x = 0; x < 4; ++x)
           if (live)
-            dst[x] = make_uint4(pack_bf16x2(v[8 * x] * sc, v[8 * x + 1] * sc),
-                                pack_bf16x2(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
-                                pack_bf16x2(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
-                                pack_bf16x2(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
+            dst[x] = make_uint4(pack2<kF16>(v[8 * x] * sc, v[8 * x + 1] * sc),
+                                pack2<kF16>(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
+                                pack2<kF16>(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
+                                pack2<kF16>(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
       }
     }
   }
@@ -383,26 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   }
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_dq_d(const BwdParams &p, cudaStream_t stream) {
   using L = DqLayout<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D, kF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   LaunchProbe probe(kKindBwdDq, stream);
-  fa_bwd_dq_kernel<D><<<p.sh.tq * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
+  fa_bwd_dq_kernel<D, kF16><<<p.sh.tq * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream) {
-  if (p.sh.d == 64) return launch_dq_d<64>(p, stream);
-  if (p.sh.d == 128) return launch_dq_d<128>(p, stream);
+  const bool f16 = p.sh.f16 != 0;
+  if (p.sh.d == 64) return f16 ? launch_dq_d<64, true>(p, stream) : launch_dq_d<64, false>(p, stream);
+  if (p.sh.d == 96 || p.sh.d == 128)
+    return f16 ? launch_dq_d<128, true>(p, stream) : launch_dq_d<128, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

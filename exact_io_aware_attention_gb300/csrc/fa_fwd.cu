@@ -24,7 +24,7 @@
 //   warps 8-11  softmax of Q tile 1
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S_0   [128,256) S_1   [256,256+d) O_0   [256+d,256+2d) O_1
-//   P_t (bf16 pairs): the first 64 columns of S_t (d = 128) or [384+64t, +64) (d = 64)
+//   P_t (16-bit pairs): the first 64 columns of S_t (d = 128) or [384+64t, +64) (d = 64)
 // The MMA issue order PV_0(n), S_0(n+1), PV_1(n), S_1(n+1) lets the tensor
 // core work on one Q tile while the other tile's softmax runs.
 //
@@ -63,7 +63,7 @@ struct FwdLayout {
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
   static_assert(kAlloc <= 232448, "shared memory budget");
-  // P_t (bf16 pairs, 64 columns) lives in tensor memory as the A operand of
+  // P_t (16-bit pairs, 64 columns) lives in tensor memory as the A operand of
   // O_t += P_t V. With d = 128 the 512 columns hold S_0, S_1, O_0, O_1 and P_t
   // takes the first half of S_t's columns once S_t has been read; with d = 64
   // it has columns of its own.
@@ -92,8 +92,11 @@ enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 
 // kSplit: the keys are split over p.n_split CTAs per Q-tile pair and the
 // epilogue writes this split's partial result (a separate instantiation, so
-// the plain forward carries none of it).
-template <int D, bool kSplit>
+// the plain forward carries none of it). kF16: f16 elements instead of bf16
+// (Q, K, V, P and a 16-bit O). D is 64 or 128; a head dimension of 96 runs
+// as 128, the tensor maps reading zeros in columns 96..127, and only the
+// first sh.d columns are stored.
+template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -229,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else if (warp == 1) {
     // ---- tcgen05 issuer ----------------------------------------------------
     if (elect_one()) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, 0, 0);  // Q K^T, both K-major
-      constexpr uint32_t kIdPV = idesc_bf16_f32(kTile, D, 0, 1);     // P V, V is MN-major
+      constexpr uint32_t kIdS = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // Q K^T, both K-major
+      constexpr uint32_t kIdPV = idesc_f32acc(kTile, D, 0, 1, kF16);     // P V, V is MN-major
       bool ok = count == 0 || mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
       uint32_t pcount[2] = {0, 0};
       bool first_pv[2] = {true, true};
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + t * kTile, sdesc_sw128(q_base + off, 16, 1024),
+          mma_f16kind_ss(tmem + t * kTile, sdesc_sw128(q_base + off, 16, 1024),
                       sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
         }
       };
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const uint32_t v_base = sKV + vslot * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
+          mma_f16kind_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
                       sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
                       (kk > 0 || !first) ? 1u : 0u);
       };
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           m_used = m_tile;
         }
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-        // P = exp2(s*c - m) -> bf16 pairs (keys 2x, 2x+1 in column x) in tensor
+        // P = exp2(s*c - m) -> 16-bit pairs (keys 2x, 2x+1 in column x) in tensor
         // memory; the row sum uses 4 independent partial sums
         float lp[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk0[32], pk1[32];
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const float p0 = ex2_approx(fmaf(s[2 * x], c, -m_sub));
           const float p1 = ex2_approx(fmaf(s[2 * x + 1], c, -m_sub));
           lp[x & 3] += p0 + p1;
-          pk0[x] = pack_bf16x2(p0, p1);
+          pk0[x] = pack2<kF16>(p0, p1);
         }
         tmem_st32(tP, pk0);
 #pragma unroll
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
           const float p1 = ex2_approx(fmaf(s[64 + 2 * x + 1], c, -m_sub));
           lp[x & 3] += p0 + p1;
-          pk1[x] = pack_bf16x2(p0, p1);
+          pk1[x] = pack2<kF16>(p0, p1);
         }
         tmem_st32(tP + 32, pk1);
         l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
@@ -420,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
+          if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
           uint32_t o[32];
           if (any) {
             tmem_ld32(tO + q * 32, o);
@@ -442,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
               uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l);
+              v.x = pack2<kF16>(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l);
+              v.y = pack2<kF16>(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l);
+              v.z = pack2<kF16>(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l);
+              v.w = pack2<kF16>(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l);
               dst[x] = v;
             }
           }
@@ -470,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 // Merge of the n_split partial results of one query row (see the top of the
 // file): thread = 8 consecutive columns of a row; the row's n_split LSE values
 // are read by each of its D/8 threads (L1 broadcast). HBM-bound:
-// n_split * (4d + 4) bytes read and 2d + 4 (bf16 O) written per row.
-template <int D>
+// n_split * (4d + 4) bytes read and 2d + 4 (16-bit O) written per row.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(256) fa_fwd_combine(const __grid_constant__ FwdParams p) {
   constexpr int kLanes = D / 8;
   const Shape &sh = p.sh;
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(256) fa_fwd_combine(const __grid_constant__ Fw
   const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t row = gt / kLanes;  // bh * nq + n
   const int part = int(gt % kLanes);
-  if (row >= rows) return;
+  if (row >= rows || part * 8 >= sh.d) return;
   float m = -INFINITY;
   for (int s = 0; s < p.n_split; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -505,22 +509,22 @@ __global__ void __launch_bounds__(256) fa_fwd_combine(const __grid_constant__ Fw
     o[1] = make_float4(acc[4] * inv_l, acc[5] * inv_l, acc[6] * inv_l, acc[7] * inv_l);
   } else {
     *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + dst) =
-        make_uint4(pack_bf16x2(acc[0] * inv_l, acc[1] * inv_l), pack_bf16x2(acc[2] * inv_l, acc[3] * inv_l),
-                   pack_bf16x2(acc[4] * inv_l, acc[5] * inv_l), pack_bf16x2(acc[6] * inv_l, acc[7] * inv_l));
+        make_uint4(pack2<kF16>(acc[0] * inv_l, acc[1] * inv_l), pack2<kF16>(acc[2] * inv_l, acc[3] * inv_l),
+                   pack2<kF16>(acc[4] * inv_l, acc[5] * inv_l), pack2<kF16>(acc[6] * inv_l, acc[7] * inv_l));
   }
   if (part == 0) p.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   using L = FwdLayout<D>;
   static bool configured = false;  // attribute set once per process (idempotent anyway)
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, false>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, false, kF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_fwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               L::kAlloc);
+      e = cudaFuncSetAttribute(fa_fwd_kernel<D, true, kF16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -528,16 +532,16 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   {
     LaunchProbe probe(kKindFwd, stream);
     if (p.n_split > 1)
-      fa_fwd_kernel<D, true><<<grid, kThreads, L::kAlloc, stream>>>(p);
+      fa_fwd_kernel<D, true, kF16><<<grid, kThreads, L::kAlloc, stream>>>(p);
     else
-      fa_fwd_kernel<D, false><<<grid, kThreads, L::kAlloc, stream>>>(p);
+      fa_fwd_kernel<D, false, kF16><<<grid, kThreads, L::kAlloc, stream>>>(p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split == 1) return e;
   const size_t threads = (size_t)p.sh.bh * p.sh.nq * (D / 8);
   {
     LaunchProbe probe(kKindFwdCombine, stream);
-    fa_fwd_combine<D><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
+    fa_fwd_combine<D, kF16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
@@ -545,8 +549,10 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream) {
-  if (p.sh.d == 64) return launch_fwd_d<64>(p, stream);
-  if (p.sh.d == 128) return launch_fwd_d<128>(p, stream);
+  const bool f16 = p.sh.f16 != 0;
+  if (p.sh.d == 64) return f16 ? launch_fwd_d<64, true>(p, stream) : launch_fwd_d<64, false>(p, stream);
+  if (p.sh.d == 96 || p.sh.d == 128)
+    return f16 ? launch_fwd_d<128, true>(p, stream) : launch_fwd_d<128, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -29,7 +29,8 @@ struct RowStrides {
 struct Shape {
   int bh, heads;                      // B*H and H (bh = b * heads + h)
   int nq, nk, tq, tk;
-  int d, causal, causal_off;
+  int d, causal, causal_off;          // d: the head dimension (the kernels run 96 as 128)
+  int f16;                            // 16-bit element type: 1 = f16, 0 = bf16
   const uint8_t *mask;                // [tq][tk] or null
 
   // Largest K/V tile with a key visible to some row of Q tile i, or -1.
@@ -65,11 +66,12 @@ struct Shape {
 };
 
 struct FwdParams {
-  // 4-D bf16 maps over [B][H][rows][d] (dims d, rows, H, B), box 64 x 128 x 1 x 1,
-  // 128-byte swizzle; rows past the end of a head read zeros
+  // 4-D maps over [B][H][rows][d] (dims d, rows, H, B) of bf16 or f16 elements,
+  // box 64 x 128 x 1 x 1, 128-byte swizzle; rows past the end of a head and
+  // columns past d read zeros
   CUtensorMap tm_q, tm_k, tm_v;
   Shape sh;
-  void *o;                            // bf16 or fp32 rows, strides so
+  void *o;                            // 16-bit (the inputs' type) or fp32 rows, strides so
   RowStrides so;
   float *lse;                         // [B*H][nq]
   int o_f32;                          // 1: O stored as fp32
@@ -87,12 +89,12 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
   Shape sh;
-  const void *o, *dout;               // bf16 rows, strides so / sdo
+  const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;
   const float *lse;                   // [B*H][nq]
   float *delta;                       // workspace: D_i, [B*H][tq*128]
   float *lse2;                        // workspace: LSE_i * log2(e), [B*H][tq*128]
-  void *dq, *dk, *dv;                 // bf16 outputs, strides sdq / sdk / sdv
+  void *dq, *dk, *dv;                 // 16-bit outputs, strides sdq / sdk / sdv
   RowStrides sdq, sdk, sdv;
   int head_group;                     // CTA order: heads per group (1..bh)
   float scale, scale_log2;

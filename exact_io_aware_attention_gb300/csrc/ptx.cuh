@@ -175,8 +175,9 @@ __device__ __forceinline__ void tc_fence_after() {
 // ---------------------------------------------------------------------------
 // tcgen05: MMA issue (one thread) and completion tracking
 
-// D[tmem] (+)= A[smem] * B[smem]; kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]; kind::f16 (bf16 or f16 inputs as the instruction
+// descriptor says, fp32 accumulate).
+__device__ __forceinline__ void mma_f16kind_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -187,7 +188,7 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 }
 
 // D[tmem] (+)= A[tmem] * B[smem].
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16kind_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -204,13 +205,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   15 A major (0 = K-major, 1 = MN-major), 16 B major, 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,
-                                                      int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |
-         (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// Instruction descriptor for kind::f16 with fp32 D and A, B both bf16
+// (f16 = false) or both f16 (f16 = true).
+//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16, 1 = bf16), 10-12 B
+//   format, 15 A major (0 = K-major, 1 = MN-major), 16 B major, 17-22 N >> 3,
+//   24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn_major, int b_mn_major,
+                                                    bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -298,6 +302,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 values rounded to the 16-bit element type (round to nearest even)
+// and packed, `lo` in the low half.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+// The two 16-bit elements of `w` widened to fp32 (exact), low half first.
+template <bool kF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+  if (kF16) {
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+  } else {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  }
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -6,7 +6,8 @@ inputs (bf16 values widen exactly to float64).
 
 Recipe:
   * Q, K, V, dO: iid N(0, 1) fp32 from ``torch.Generator('cpu').manual_seed``,
-    rounded to bf16 with round-to-nearest-even (``.to(torch.bfloat16)``).
+    rounded to bf16 with round-to-nearest-even (``.to(torch.bfloat16)``), or
+    to fp16 the same way where a test asks for fp16 inputs.
   * seed = 1000 * case + tensor index, with Q = 0, K = 1, V = 2, dO = 3,
     mask = 4 (``case`` numbers the workloads listed in ``WORKLOADS``).
   * block mask: ``T x T`` uint8 with T = N / 128, every diagonal tile kept and
@@ -58,11 +59,12 @@ def seed_for(case: int, tensor: str) -> int:
     return SEED_STRIDE * case + TENSOR_INDEX[tensor]
 
 
-def normal_bf16(shape, seed: int) -> torch.Tensor:
-    """iid N(0,1) drawn in fp32 on the CPU from ``seed``, rounded to bf16 (RNE)."""
+def normal_bf16(shape, seed: int, dtype=torch.bfloat16) -> torch.Tensor:
+    """iid N(0,1) drawn in fp32 on the CPU from ``seed``, rounded to bf16 (RNE),
+    or to ``dtype`` (fp16)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(dtype)
 
 
 def block_mask(n_tiles: int, density: float, seed: int, n_key_tiles: int | None = None):
@@ -76,14 +78,15 @@ def block_mask(n_tiles: int, density: float, seed: int, n_key_tiles: int | None 
     return keep.to(torch.uint8)
 
 
-def make_inputs(B, H, N, d, case: int, with_do: bool = True, Nk: int | None = None):
-    """CPU bf16 tensors q (and do) of shape [B, H, N, d], k and v of shape
-    [B, H, Nk, d] (Nk = N by default)."""
+def make_inputs(B, H, N, d, case: int, with_do: bool = True, Nk: int | None = None,
+                dtype=torch.bfloat16):
+    """CPU tensors q (and do) of shape [B, H, N, d], k and v of shape
+    [B, H, Nk, d] (Nk = N by default), bf16 or ``dtype``."""
     nk = N if Nk is None else Nk
-    out = {t: normal_bf16((B, H, N if t in ("q", "do") else nk, d), seed_for(case, t))
+    out = {t: normal_bf16((B, H, N if t in ("q", "do") else nk, d), seed_for(case, t), dtype)
            for t in ("q", "k", "v")}
     if with_do:
-        out["do"] = normal_bf16((B, H, N, d), seed_for(case, "do"))
+        out["do"] = normal_bf16((B, H, N, d), seed_for(case, "do"), dtype)
     return out
 
 

@@ -22,17 +22,19 @@
  *    contiguous row-major [B][H][N][d] tensors with Nq = Nk = N; the _ex entry
  *    points take an fa_tensor descriptor per operand (any strides over b, h
  *    and the row, e.g. the [B][N][H][d] layout) and separate Nq and Nk.
- *    Q, K, V, dO, dQ, dK, dV hold bf16 values (raw 16-bit storage); O is bf16
- *    (fp32 through fa_forward_f32 or an FA_F32 descriptor). LSE is fp32
- *    contiguous [B][H][Nq], the natural-log log-sum-exp of the scaled scores
- *    of each query row.
+ *    Q, K, V, dO, dQ, dK, dV hold 16-bit values of one type: bf16 (the plain
+ *    entry points; FA_BF16) or f16 (FA_F16, _ex entry points only). O has
+ *    that type too, or fp32 (fa_forward_f32 or an FA_F32 descriptor). The
+ *    tensor cores multiply in that 16-bit type (P and dS are rounded to it)
+ *    and accumulate in fp32. LSE is fp32 contiguous [B][H][Nq], the
+ *    natural-log log-sum-exp of the scaled scores of each query row.
  *  - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
  *    caller. The library never allocates, frees or synchronises; all work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *    default stream), which must belong to the device that holds Q. Each call
  *    makes that device current on the calling thread. Inputs are only read;
  *    outputs must not overlap one another or an input.
- *  - Supported: d in {64, 128}; 1 <= Nq, Nk <= 65536 (any length: a last,
+ *  - Supported: d in {64, 96, 128}; 1 <= Nq, Nk <= 65536 (any length: a last,
  *    partial tile of 128 rows is handled inside the kernels); B, H >= 1;
  *    B*H*max(Nq, Nk) <= 2^31 - 1; scale finite and > 0. B*H*Nq == 0 is a
  *    no-op that returns FA_OK; Nk == 0 with Nq > 0 is FA_ERR_UNSUPPORTED.
@@ -66,7 +68,8 @@ extern "C" {
 /* Element types of an fa_tensor. */
 typedef enum fa_dtype {
   FA_BF16 = 0, /* bfloat16, raw 16-bit storage */
-  FA_F32 = 1   /* IEEE fp32 (accepted for O only) */
+  FA_F32 = 1,  /* IEEE fp32 (accepted for O only) */
+  FA_F16 = 2   /* IEEE binary16, raw 16-bit storage */
 } fa_dtype;
 
 /*
@@ -130,7 +133,8 @@ fa_status fa_forward_f32(const void *Q, const void *K, const void *V, float *O, 
 
 /*
  * Forward pass on strided operands with Nq query rows and Nk keys per
- * (batch, head). Q, K, V are FA_BF16; O is FA_BF16 or FA_F32; LSE is fp32
+ * (batch, head). Q, K, V are all FA_BF16 or all FA_F16; O has their type or
+ * is FA_F32; LSE is fp32
  * contiguous [B,H,Nq]. Errors as for fa_forward, plus FA_ERR_UNSUPPORTED or
  * FA_ERR_MISALIGNED for a descriptor outside the rules of fa_tensor
  * (fa_last_error() names the operand).
@@ -197,7 +201,7 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
 /*
  * Backward pass on strided operands with Nq query rows and Nk keys per
  * (batch, head): Q, O, dO, dQ have Nq rows, K, V, dK, dV have Nk rows, all
- * FA_BF16; LSE is fp32 contiguous [B,H,Nq] as written by fa_forward_ex with
+ * FA_BF16 or all FA_F16; LSE is fp32 contiguous [B,H,Nq] as written by fa_forward_ex with
  * the same arguments. The workspace holds at least
  * fa_backward_workspace_bytes(B,H,Nq,d) bytes, 256-byte aligned.
  */

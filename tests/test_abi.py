@@ -69,7 +69,7 @@ def fwd(lib, q=A, k=A, v=A, o=B_, lse=B_, B=1, H=1, N=256, d=64, causal=0, scale
     (dict(B=-1), INVALID), (dict(N=-128), INVALID), (dict(d=0), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(scale=float("nan")), INVALID),
-    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(N=65537), UNSUPPORTED),
+    (dict(d=80), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(N=65537), UNSUPPORTED),
     (dict(N=128 * 513), UNSUPPORTED),
     (dict(B=65536, H=256, N=256), UNSUPPORTED),
     (dict(q=M), MISALIGNED), (dict(v=M), MISALIGNED), (dict(lse=M), MISALIGNED),
@@ -136,7 +136,9 @@ PASSED_HOST_CHECKS = (INVALID, 4)
     (dict(v=desc(sn=-64)), UNSUPPORTED),                  # negative stride
     (dict(q=desc(sn=0)), UNSUPPORTED),                    # zero stride of a long dimension
     (dict(q=desc(sn=1 << 40)), UNSUPPORTED),              # beyond the tensor-map range
-    (dict(q=desc(dtype=2)), UNSUPPORTED),                 # an element type the kernels lack
+    (dict(q=desc(dtype=3)), UNSUPPORTED),                 # an element type the kernels lack
+    (dict(q=desc(dtype=binding.FA_F16)), UNSUPPORTED),    # f16 Q with bf16 K and V
+    (dict(q=desc(dtype=binding.FA_F32)), UNSUPPORTED),    # fp32 inputs
     (dict(o=desc(ptr=B_, dtype=7)), UNSUPPORTED),
     (dict(q=desc(reserved=1)), INVALID),
     (dict(q=desc(ptr=None)), INVALID),
@@ -156,6 +158,11 @@ def test_forward_ex_rejects_bad_descriptors(lib, case, status):
     dict(q=desc(sn=2 * 64, sh=64, sb=300 * 2 * 64)),               # [B, N, H, d] layout
     dict(o=desc(ptr=B_, dtype=binding.FA_F32, sn=64, sh=300 * 64)),  # fp32 O
     dict(B=1, q=desc(sb=3)),                                       # stride of a length-1 dim
+    dict(d=96),                                                    # head dimension 96
+    dict(q=desc(dtype=binding.FA_F16), k=desc(dtype=binding.FA_F16),  # fp16 throughout
+         v=desc(dtype=binding.FA_F16), o=desc(ptr=B_, dtype=binding.FA_F16)),
+    dict(q=desc(dtype=binding.FA_F16), k=desc(dtype=binding.FA_F16),  # fp16 in, fp32 O
+         v=desc(dtype=binding.FA_F16), o=desc(ptr=B_, dtype=binding.FA_F32)),
 ])
 def test_forward_ex_accepts_general_shapes(lib, case):
     assert fwd_ex(lib, **case) in PASSED_HOST_CHECKS
