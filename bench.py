@@ -377,7 +377,7 @@ def run_cuda(args, dist: Dist):
                 "dq_kernel_ms": round(avg("fa_bwd_dq"), 4),
                 "dq_kernel_executed_tflops": round(0.6 * bwd_fl / avg("fa_bwd_dq") / 1e9, 1)
                 if per_kernel["fa_bwd_dq"][1] else None},
-        "per_kernel_ms": {kname: round(t / n, 4) if n else None for kname, (t, n) in per_kernel.items()},
+        "per_kernel_ms": {kname: round(t / n, 4) for kname, (t, n) in per_kernel.items() if n},
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
