@@ -146,8 +146,18 @@ def _mask(block_mask, nq, nk):
 def default_num_splits(B, H, Nq, Nk, d, causal, device=None) -> int:
     """The library's choice of key splits for the forward pass of this shape
     (1: no split) on ``device`` (default: the current CUDA device)."""
-    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+    dev = torch.device(device) if device is not None else None
+    if dev is None or dev.index is None or dev.index == torch.cuda.current_device():
         return int(load_library().fa_forward_num_splits(B, H, Nq, Nk, d, int(bool(causal))))
+    with torch.cuda.device(dev):
+        return int(load_library().fa_forward_num_splits(B, H, Nq, Nk, d, int(bool(causal))))
+
+
+def _fills_gpu(B, H, Nq, device) -> bool:
+    """Whether the plain forward's grid (one CTA per pair of 128-row query
+    tiles and head) already gives every SM a CTA, so no split can help."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return ((-(-Nq // 128) + 1) // 2) * B * H >= sms
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mask=None,
@@ -179,7 +189,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
     dq_, dk_, dv_, do_ = (_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
     lib = load_library()
     if num_splits is None:
-        num_splits = default_num_splits(B, H, Nq, Nk, d, causal, q.device)
+        num_splits = 1 if _fills_gpu(B, H, Nq, q.device) else \
+            default_num_splits(B, H, Nq, Nk, d, causal, q.device)
     if num_splits == 1:
         _check(lib.fa_forward_ex(
             ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_),

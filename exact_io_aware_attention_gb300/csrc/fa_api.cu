@@ -227,6 +227,22 @@ size_t split_lse_bytes(int B, int H, int Nq, int ns) {
 
 constexpr int kMaxSplits = 128;
 
+// SM count of the calling thread's current device, looked up once per device
+// (0 if unknown).
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
+
 fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
                        const fa_tensor *O, float *LSE, int B, int H, int Nq, int Nk, int d,
                        int causal, float scale, const uint8_t *block_mask, int n_split,
@@ -525,10 +541,8 @@ int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal) {
   (void)d;
   bool empty;
   if (check_shape(B, H, Nq, Nk, 64, 1.f, &empty) != FA_OK || empty) return 1;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    return 1;
+  const int sms = sm_count();
+  if (sms <= 0) return 1;
   const fa::Shape sh = make_shape(B, H, Nq, Nk, 64, causal, nullptr);
   const long long ctas = (long long)((sh.tq + 1) / 2) * sh.bh;  // one CTA per SM is resident
   // K/V tiles the pair with the most work visits
