@@ -153,11 +153,13 @@ def default_num_splits(B, H, Nq, Nk, d, causal, device=None) -> int:
         return int(load_library().fa_forward_num_splits(B, H, Nq, Nk, d, int(bool(causal))))
 
 
-def _fills_gpu(B, H, Nq, device) -> bool:
+def _fills_gpu(B, H, Nq, d, device) -> bool:
     """Whether the plain forward's grid (one CTA per pair of 128-row query
-    tiles and head) already gives every SM a CTA, so no split can help."""
+    tiles and head; one per tile for d = 256) already gives every SM a CTA,
+    so no split can help."""
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    return ((-(-Nq // 128) + 1) // 2) * B * H >= sms
+    tiles = -(-Nq // 128)
+    return (tiles if d == 256 else (tiles + 1) // 2) * B * H >= sms
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mask=None,
@@ -189,7 +191,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
     dq_, dk_, dv_, do_ = (_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
     lib = load_library()
     if num_splits is None:
-        num_splits = 1 if _fills_gpu(B, H, Nq, q.device) else \
+        num_splits = 1 if _fills_gpu(B, H, Nq, d, q.device) else \
             default_num_splits(B, H, Nq, Nk, d, causal, q.device)
     if num_splits == 1:
         _check(lib.fa_forward_ex(

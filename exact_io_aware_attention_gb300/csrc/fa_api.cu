@@ -163,11 +163,13 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Shape checks shared by every entry point; `*empty` is set for a no-op call.
-fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *empty) {
+// Head dimension 256 has a forward pass only.
+fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *empty,
+                      bool backward = false) {
   *empty = false;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && (d != 256 || backward)) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H * Nq == 0) {
     *empty = true;
     return FA_OK;
@@ -310,7 +312,7 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
                         const uint8_t *block_mask, void *workspace, size_t ws_bytes,
                         void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty);
+  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty, true);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
@@ -538,13 +540,14 @@ fa_status fa_forward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
 }
 
 int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal) {
-  (void)d;
   bool empty;
   if (check_shape(B, H, Nq, Nk, 64, 1.f, &empty) != FA_OK || empty) return 1;
   const int sms = sm_count();
   if (sms <= 0) return 1;
   const fa::Shape sh = make_shape(B, H, Nq, Nk, 64, causal, nullptr);
-  const long long ctas = (long long)((sh.tq + 1) / 2) * sh.bh;  // one CTA per SM is resident
+  // CTAs of the plain forward (one per SM is resident): a pair of Q tiles
+  // per CTA, one with head dimension 256
+  const long long ctas = (long long)(d == 256 ? sh.tq : (sh.tq + 1) / 2) * sh.bh;
   // K/V tiles the pair with the most work visits
   const int tiles = sh.last_kv_tile(sh.tq - 1) + 1;
   if (ctas >= sms || tiles < 4) return 1;
@@ -629,7 +632,7 @@ fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const
                               int B, int H, int N, int d, int causal, float scale,
                               const uint8_t *block_mask, void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, N, N, d, scale, &empty);
+  fa_status s = check_shape(B, H, N, N, d, scale, &empty, true);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
   const size_t need = fa_backward_workspace_bytes(B, H, N, d);

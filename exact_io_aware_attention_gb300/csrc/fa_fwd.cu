@@ -516,6 +516,14 @@ __global__ void __launch_bounds__(256) fa_fwd_combine(const __grid_constant__ Fw
 }
 
 template <int D, bool kF16>
+cudaError_t launch_combine(const FwdParams &p, cudaStream_t stream) {
+  const size_t threads = (size_t)p.sh.bh * p.sh.nq * (D / 8);
+  LaunchProbe probe(kKindFwdCombine, stream);
+  fa_fwd_combine<D, kF16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, bool kF16>
 cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   using L = FwdLayout<D>;
   static bool configured = false;  // attribute set once per process (idempotent anyway)
@@ -538,12 +546,7 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split == 1) return e;
-  const size_t threads = (size_t)p.sh.bh * p.sh.nq * (D / 8);
-  {
-    LaunchProbe probe(kKindFwdCombine, stream);
-    fa_fwd_combine<D, kF16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  return launch_combine<D, kF16>(p, stream);
 }
 
 }  // namespace
@@ -553,6 +556,11 @@ cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream) {
   if (p.sh.d == 64) return f16 ? launch_fwd_d<64, true>(p, stream) : launch_fwd_d<64, false>(p, stream);
   if (p.sh.d == 96 || p.sh.d == 128)
     return f16 ? launch_fwd_d<128, true>(p, stream) : launch_fwd_d<128, false>(p, stream);
+  if (p.sh.d == 256) {  // its own kernel (fa_fwd_d256.cu); the merge is shared
+    cudaError_t e = launch_forward_d256(p, stream);
+    if (e != cudaSuccess || p.n_split == 1) return e;
+    return f16 ? launch_combine<256, true>(p, stream) : launch_combine<256, false>(p, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

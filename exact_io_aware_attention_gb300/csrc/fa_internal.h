@@ -123,6 +123,7 @@ class LaunchProbe {
 constexpr uint32_t kDebugSkipLoads = 1u;
 
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);  // + the merge when split
+cudaError_t launch_forward_d256(const FwdParams &p, cudaStream_t stream);  // fa_fwd_d256.cu
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_bwd_dq.cu
 

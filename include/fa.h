@@ -34,7 +34,8 @@
  *    default stream), which must belong to the device that holds Q. Each call
  *    makes that device current on the calling thread. Inputs are only read;
  *    outputs must not overlap one another or an input.
- *  - Supported: d in {64, 96, 128}; 1 <= Nq, Nk <= 65536 (any length: a last,
+ *  - Supported: d in {64, 96, 128}, and d = 256 for the forward entry points
+ *    (the backward returns FA_ERR_UNSUPPORTED for it); 1 <= Nq, Nk <= 65536 (any length: a last,
  *    partial tile of 128 rows is handled inside the kernels); B, H >= 1;
  *    B*H*max(Nq, Nk) <= 2^31 - 1; scale finite and > 0. B*H*Nq == 0 is a
  *    no-op that returns FA_OK; Nk == 0 with Nq > 0 is FA_ERR_UNSUPPORTED.

@@ -69,7 +69,7 @@ def fwd(lib, q=A, k=A, v=A, o=B_, lse=B_, B=1, H=1, N=256, d=64, causal=0, scale
     (dict(B=-1), INVALID), (dict(N=-128), INVALID), (dict(d=0), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(scale=float("nan")), INVALID),
-    (dict(d=80), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(N=65537), UNSUPPORTED),
+    (dict(d=80), UNSUPPORTED), (dict(d=512), UNSUPPORTED), (dict(N=65537), UNSUPPORTED),
     (dict(N=128 * 513), UNSUPPORTED),
     (dict(B=65536, H=256, N=256), UNSUPPORTED),
     (dict(q=M), MISALIGNED), (dict(v=M), MISALIGNED), (dict(lse=M), MISALIGNED),
@@ -229,3 +229,10 @@ def test_split_forward_rejects_bad_arguments(lib):
     assert split_fwd(lib, 4, ws=ctypes.c_void_p(0x20010)) == MISALIGNED
     assert split_fwd(lib, 4) in PASSED_HOST_CHECKS
     assert split_fwd(lib, 1, ws=None, ws_bytes=0) in PASSED_HOST_CHECKS  # no split: no workspace
+
+
+def test_head_dim_256_is_forward_only(lib):
+    assert fwd_ex(lib, d=256) in PASSED_HOST_CHECKS
+    assert bwd(lib, d=256) == UNSUPPORTED
+    assert lib.fa_backward_noalloc(A, A, A, A, A, A, B_, B_, B_, 1, 1, 256, 256, 0, 0.1, None,
+                                   None) == UNSUPPORTED
