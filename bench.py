@@ -171,9 +171,20 @@ def summarize_clocks(rows):
             "power_w_max": max(power) if power else None}
 
 
-def kernel_source_hash():
+# Source files each measured kernel is compiled from (its own file and the
+# shared headers): a committed ncu capture is valid while they are unchanged.
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
+    "fa_bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+    "fa_bwd_dq": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str | None = None):
+    """sha256 prefix of the sources of `kernel` (of all measured kernels when None)."""
+    files = KERNEL_SOURCES[kernel] if kernel else sorted({f for v in KERNEL_SOURCES.values() for f in v})
     h = hashlib.sha256()
-    for f in ("fa_bwd.cu", "fa_bwd_dq.cu", "fa_fwd.cu", "ptx.cuh", "fa_internal.h"):
+    for f in files:
         with open(os.path.join(ROOT, "exact_io_aware_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -181,13 +192,13 @@ def kernel_source_hash():
 
 def dram_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the summary is missing or the kernels changed since."""
+    None when the summary is missing or the kernel's sources changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         entry = t["kernels"][kernel]
-        if t.get("source_hash") != kernel_source_hash():
+        if entry.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(entry["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError, TypeError):
