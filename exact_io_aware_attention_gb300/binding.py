@@ -93,14 +93,27 @@ def load_library(path: str | None = None):
     return _lib
 
 
+def _lib_fast():
+    return _lib if _lib is not None else load_library()
+
+
 def _check(status: int, what: str):
     if status != FA_OK:
         detail = load_library().fa_last_error().decode()
         raise FAError(status, what, detail)
 
 
-def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(device=None):
+    """The current CUDA stream of `device` (default: the current device) as a
+    raw handle."""
+    if _raw_stream is not None:
+        idx = device.index if device is not None and device.index is not None else \
+            torch.cuda.current_device()
+        return ctypes.c_void_p(_raw_stream(idx))
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
 def _ptr(t):
@@ -109,26 +122,28 @@ def _ptr(t):
 
 def _desc(t, name):
     """fa_tensor of a [B, H, rows, d] CUDA tensor whose d elements are contiguous."""
-    if not t.is_cuda or t.dim() != 4:
-        raise ValueError(f"{name} must be a 4-D CUDA tensor [B, H, rows, d]")
-    if t.dtype not in _DTYPES:
-        raise ValueError(f"{name}: dtype {t.dtype} is not supported")
-    if t.stride(3) != 1 and t.shape[3] > 1:
-        raise ValueError(f"{name}: the last dimension must be contiguous")
-    return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2), _DTYPES[t.dtype], 0)
+    dt = _DTYPES.get(t.dtype)
+    st = t.stride()
+    if not t.is_cuda or len(st) != 4 or dt is None or (st[3] != 1 and t.shape[3] > 1):
+        raise ValueError(f"{name} must be a 4-D CUDA tensor [B, H, rows, d] of a supported "
+                         f"dtype with contiguous rows (got {tuple(t.shape)}, {t.dtype}, {st})")
+    return FaTensor(t.data_ptr(), st[0], st[1], st[2], dt, 0)
 
 
 def _shapes(q, kv, qlike=()):
     """(B, H, Nq, Nk, d) of q [B,H,Nq,d] and k, v [B,H,Nk,d]."""
-    if q.dim() != 4:
+    qs = q.shape
+    if len(qs) != 4:
         raise ValueError("q must be [B, H, Nq, d]")
-    B, H, Nq, d = q.shape
-    Nk = kv[0].shape[2] if kv[0].dim() == 4 else -1
+    B, H, Nq, d = qs
+    ks = kv[0].shape
+    Nk = ks[2] if len(ks) == 4 else -1
     for t in kv:
-        if t.dim() != 4 or tuple(t.shape) != (B, H, Nk, d):
+        ts = t.shape
+        if len(ts) != 4 or ts[0] != B or ts[1] != H or ts[2] != Nk or ts[3] != d:
             raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
     for t in qlike:
-        if tuple(t.shape) != (B, H, Nq, d):
+        if t.shape != qs:
             raise ValueError("o and do must have q's shape")
     return B, H, Nq, Nk, d
 
@@ -153,11 +168,17 @@ def default_num_splits(B, H, Nq, Nk, d, causal, device=None) -> int:
         return int(load_library().fa_forward_num_splits(B, H, Nq, Nk, d, int(bool(causal))))
 
 
+_sm_counts = {}
+
+
 def _fills_gpu(B, H, Nq, d, device) -> bool:
     """Whether the plain forward's grid (one CTA per pair of 128-row query
     tiles and head; one per tile for d = 256) already gives every SM a CTA,
     so no split can help."""
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    sms = _sm_counts.get(idx)
+    if sms is None:
+        sms = _sm_counts[idx] = torch.cuda.get_device_properties(idx).multi_processor_count
     tiles = -(-Nq // 128)
     return (tiles if d == 256 else (tiles + 1) // 2) * B * H >= sms
 
@@ -185,32 +206,32 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
         out = torch.empty_like(q, dtype=q.dtype if o_dtype is None else o_dtype)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    if tuple(out.shape) != (B, H, Nq, d) or tuple(lse.shape) != (B, H, Nq) or \
+    if out.shape != q.shape or lse.shape != (B, H, Nq) or \
             lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("out must be [B, H, Nq, d] and lse contiguous fp32 [B, H, Nq]")
-    dq_, dk_, dv_, do_ = (_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
-    lib = load_library()
+    dq_, dk_, dv_, do_ = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out")
+    lib = _lib_fast()
     if num_splits is None:
         num_splits = 1 if _fills_gpu(B, H, Nq, d, q.device) else \
             default_num_splits(B, H, Nq, Nk, d, causal, q.device)
     if num_splits == 1:
         _check(lib.fa_forward_ex(
             ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_),
-            _ptr(lse), B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), _stream()),
-            "fa_forward_ex")
+            _ptr(lse), B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask),
+            _stream(q.device)), "fa_forward_ex")
         return out, lse
     nbytes = int(lib.fa_forward_split_workspace_bytes(B, H, Nq, d, int(num_splits)))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     _check(lib.fa_forward_split_ex(
         ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
         B, H, Nq, Nk, d, int(bool(causal)), scale, _ptr(mask), int(num_splits), _ptr(ws),
-        nbytes, _stream()), "fa_forward_split_ex")
+        nbytes, _stream(q.device)), "fa_forward_split_ex")
     return out, lse
 
 
 def backward_workspace_bytes(B, H, N, d) -> int:
     """Workspace bytes of the backward pass for N query rows per (batch, head)."""
-    return int(load_library().fa_backward_workspace_bytes(B, H, N, d))
+    return int(_lib_fast().fa_backward_workspace_bytes(B, H, N, d))
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
@@ -231,18 +252,16 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    if tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape) or \
-            tuple(dv.shape) != tuple(v.shape):
+    if dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape:
         raise ValueError("dq, dk, dv must have the shapes of q, k, v")
-    if tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, Nq]")
-    ds = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"),
-                                   (dq, "dq"), (dk, "dk"), (dv, "dv"))]
-    r = [ctypes.byref(x) for x in ds]
-    _check(load_library().fa_backward_ex(
+    r = [ctypes.byref(_desc(t, n)) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"),
+                                                (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    _check(_lib_fast().fa_backward_ex(
         r[0], r[1], r[2], r[3], r[4], _ptr(lse), r[5], r[6], r[7], B, H, Nq, Nk, d,
         int(bool(causal)), scale, _ptr(mask), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream()), "fa_backward_ex")
+        workspace.numel() * workspace.element_size(), _stream(q.device)), "fa_backward_ex")
     return dq, dk, dv
 
 

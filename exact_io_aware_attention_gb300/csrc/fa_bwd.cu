@@ -385,43 +385,52 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 // D_i = dO_i . O_i and LSE_i * log2(e) for every row of every Q tile: a row
 // past the end of the sequence, or one that sees no key (LSE = -inf), gets
 // D = 0 and LSE * log2(e) = +inf, which makes its P row exactly 0.
-// Thread = 8 consecutive elements of a row (16-byte loads); with a head
-// dimension of 96 (run as D = 128) the last 4 threads of a row add nothing.
+// Block = 64 rows of one head (blockIdx.x = (b * H + h) * chunks + chunk), so
+// the index arithmetic is done once per block; a row is read by 16 threads with
+// 16-byte loads (8 elements each; with a head dimension of 96, run as
+// D = 128, the last 4 threads of a row add nothing), two rows per warp step.
+constexpr int kPreRows = 64;
+
 template <int D, bool kF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdParams p) {
-  constexpr int kLanesPerRow = D / 8;
+  constexpr int kLanesPerRow = D / 8;            // 8 or 16
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const Shape &sh = p.sh;
-  const int npad = sh.tq * kTile;
-  const size_t rows = (size_t)sh.bh * npad;
-  const size_t gt = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t row = gt / kLanesPerRow;
-  const int part = int(gt % kLanesPerRow);
-  const int bh = int(row / npad), n = int(row % npad);
-  const bool live = row < rows && n < sh.nq && part * 8 < sh.d;
-  float acc = 0.f;
-  if (live) {
-    const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
-    const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.o) +
-                                                     p.so.row(b_idx, h_idx, n) + part * 8);
-    const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) +
-                                                     p.sdo.row(b_idx, h_idx, n) + part * 8);
-    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  const int chunks = sh.tq * kTile / kPreRows;  // row chunks per head
+  const int bh = int(blockIdx.x / chunks), chunk = int(blockIdx.x % chunks);
+  const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
+  const uint16_t *o_head = static_cast<const uint16_t *>(p.o) + p.so.row(b_idx, h_idx, 0);
+  const uint16_t *g_head = static_cast<const uint16_t *>(p.dout) + p.sdo.row(b_idx, h_idx, 0);
+  const size_t stat_head = (size_t)bh * sh.tq * kTile;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = lane % kLanesPerRow;
+  const bool col_live = part * 8 < sh.d;
+  for (int k = 0; k < kPreRows / (8 * kRowsPerWarp); ++k) {
+    const int n = chunk * kPreRows + (k * 8 + warp) * kRowsPerWarp + lane / kLanesPerRow;
+    const bool live = n < sh.nq;
+    float acc = 0.f;
+    if (live && col_live) {
+      const uint4 o = *reinterpret_cast<const uint4 *>(o_head + (long long)n * p.so.n_ + part * 8);
+      const uint4 g = *reinterpret_cast<const uint4 *>(g_head + (long long)n * p.sdo.n_ + part * 8);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      float o0, o1, g0, g1;
-      unpack2<kF16>(ow[h], o0, o1);
-      unpack2<kF16>(gw[h], g0, g1);
-      acc = fmaf(o0, g0, acc);
-      acc = fmaf(o1, g1, acc);
+      for (int h = 0; h < 4; ++h) {
+        float o0, o1, g0, g1;
+        unpack2<kF16>(ow[h], o0, o1);
+        unpack2<kF16>(gw[h], g0, g1);
+        acc = fmaf(o0, g0, acc);
+        acc = fmaf(o1, g1, acc);
+      }
     }
-  }
 #pragma unroll
-  for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) {
-    const float l = live ? p.lse[(size_t)bh * sh.nq + n] : -INFINITY;
-    const bool empty = isinf(l);  // also the rows past the end (l = -inf)
-    p.delta[row] = empty ? 0.f : acc;
-    p.lse2[row] = empty ? INFINITY : l * 1.4426950408889634f;
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (part == 0 && n < sh.tq * kTile) {
+      const float l = live ? p.lse[(size_t)bh * sh.nq + n] : -INFINITY;
+      const bool empty = isinf(l);  // also the rows past the end
+      p.delta[stat_head + n] = empty ? 0.f : acc;
+      p.lse2[stat_head + n] = empty ? INFINITY : l * 1.4426950408889634f;
+    }
   }
 }
 
@@ -435,11 +444,10 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const size_t rows = (size_t)p.sh.bh * p.sh.tq * kTile;
-  const size_t pre_threads = rows * (D / 8);
   {
     LaunchProbe probe(kKindBwdPre, stream);
-    fa_bwd_pre<D, kF16><<<(unsigned)((pre_threads + 255) / 256), 256, 0, stream>>>(p);
+    const unsigned blocks = unsigned(p.sh.tq * kTile / kPreRows) * unsigned(p.sh.bh);
+    fa_bwd_pre<D, kF16><<<blocks, 256, 0, stream>>>(p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
