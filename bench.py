@@ -396,6 +396,32 @@ def run_cuda(args, dist: Dist):
                "d2h_bytes_per_step": sum(outs[t].numel() * 2 for t in outs),
                "copies": "pipelined: H2D of step k+1 and D2H of step k overlap step k's compute"}
 
+    # ---- secondary ceilings: the exponential rate and HBM bytes ---------------
+    # One exp per visible score element in the forward (4 d flops each); the
+    # backward recomputes P in both of its kernels (2 exps per element).
+    # Algorithmic bytes per head: forward reads Q, K, V and writes O (16-bit)
+    # and LSE; backward reads Q, K, V, O, dO and LSE, writes dQ, dK, dV, and
+    # writes and reads D and LSE*log2(e).
+    exp2_rate = fa.measure_exp2_rate()
+    sms = props.multi_processor_count
+    mhz = clk["sm_mhz"] or peaks.get("sm_max_mhz", 2070.0)
+    peak_exps = exp2_rate * sms * mhz * 1e6
+    fwd_exps = fwd_fl / (4.0 * w.d)
+    heads = w.B * w.H
+    fwd_bytes = heads * ((3 * 2 + 2) * w.N * w.d + 4 * w.N)
+    bwd_bytes = heads * ((5 * 2 + 3 * 2) * w.N * w.d + 4 * w.N + 16 * w.N)
+    sfu = {"exp2_ops_per_clk_per_sm": round(exp2_rate, 2),
+           "peak_exps_per_s": peak_exps,
+           "fwd_exps_per_s": fwd_exps / (fwd_ms * 1e-3),
+           "fwd_frac": round(fwd_exps / (fwd_ms * 1e-3) / peak_exps, 4),
+           "bwd_exps_per_s_executed": 2 * fwd_exps / (bwd_ms * 1e-3),
+           "bwd_frac": round(2 * fwd_exps / (bwd_ms * 1e-3) / peak_exps, 4),
+           "clock_mhz": mhz}
+    hbm = {"fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1),
+           "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1),
+           "peak_gbs": peaks.get("hbm_gbs"),
+           "fwd_bytes": fwd_bytes, "bwd_bytes": bwd_bytes}
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline(w, host, budget_s=15.0)
@@ -431,6 +457,8 @@ def run_cuda(args, dist: Dist):
                      "traffic": dram_traffic(dominant),
                      "algorithmic_flops_per_launch": dom_flops},
         "e2e": e2e,
+        "sfu": sfu,
+        "hbm": hbm,
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "fa_kernel_name": ([_i], ctypes.c_char_p),
     "fa_profile_enable": ([_i], _i),
     "fa_profile_collect": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _i], _i),
+    "fa_measure_exp2_rate": ([ctypes.POINTER(ctypes.c_double)], _i),
 }
 
 _lock = threading.Lock()
@@ -273,6 +274,14 @@ def device_status(stream=None) -> int:
     if rc not in (FA_OK, 5):
         raise FAError(rc, "fa_device_status")
     return int(code.value)
+
+
+def measure_exp2_rate() -> float:
+    """ex2.approx operations per SM clock on the current device (a
+    measurement, run once; synchronises)."""
+    r = ctypes.c_double(0.0)
+    _check(_lib_fast().fa_measure_exp2_rate(ctypes.byref(r)), "fa_measure_exp2_rate")
+    return float(r.value)
 
 
 def profile_enable(enable: bool = True):

@@ -431,6 +431,42 @@ fa_status noalloc_scratch(int dev, void **out) {
   return FA_OK;
 }
 
+// ---- measurement: the SFU exp2 rate ----------------------------------------
+
+constexpr int kExpProbeThreads = 1024;
+constexpr int kExpProbeIters = 2048;
+constexpr int kExpProbeChains = 8;  // independent ex2 chains per thread
+constexpr int kMaxProbeBlocks = 1024;
+__device__ unsigned long long g_exp_probe_cycles[kMaxProbeBlocks];
+__device__ float g_exp_probe_sink[kMaxProbeBlocks];
+
+// One CTA per SM: each thread runs kExpProbeChains independent chains of
+// ex2.approx; thread 0 records the CTA's SM cycles between two block-wide
+// barriers around the loop.
+__global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
+  float a[kExpProbeChains];
+#pragma unroll
+  for (int c = 0; c < kExpProbeChains; ++c) a[c] = -1e-3f * float(threadIdx.x % 97 + c);
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < kExpProbeIters; ++it) {
+#pragma unroll
+    for (int c = 0; c < kExpProbeChains; ++c) {
+      float y;
+      asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a[c]));
+      a[c] = -y;  // stays in (-1, 0]: no overflow, and a true dependency
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < kExpProbeChains; ++c) s += a[c];
+  if (s == 12345.f) g_exp_probe_sink[blockIdx.x] = s;  // keeps the loop alive
+  if (threadIdx.x == 0 && blockIdx.x < kMaxProbeBlocks)
+    g_exp_probe_cycles[blockIdx.x] = (unsigned long long)(t1 - t0);
+}
+
 }  // namespace
 
 namespace fa {
@@ -626,6 +662,26 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 }
 
 size_t fa_backward_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+fa_status fa_measure_exp2_rate(double *ops_per_clk_per_sm) {
+  if (!ops_per_clk_per_sm) return FA_ERR_INVALID_ARG;
+  *ops_per_clk_per_sm = 0.0;
+  const int sms = sm_count();
+  if (sms <= 0 || sms > kMaxProbeBlocks) return cuda_fail("SM count", cudaErrorInvalidDevice);
+  fa_exp2_probe<<<sms, kExpProbeThreads>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("exp2 probe", e);
+  unsigned long long cycles[kMaxProbeBlocks];
+  e = cudaMemcpyFromSymbol(cycles, g_exp_probe_cycles, sizeof(unsigned long long) * sms);
+  if (e != cudaSuccess) return cuda_fail("cudaMemcpyFromSymbol", e);
+  double mean = 0.0;
+  for (int i = 0; i < sms; ++i) mean += (double)cycles[i];
+  mean /= sms;
+  if (mean <= 0.0) return cuda_fail("exp2 probe cycles", cudaErrorUnknown);
+  *ops_per_clk_per_sm = (double)kExpProbeThreads * kExpProbeIters * kExpProbeChains / mean;
+  return FA_OK;
+}
 
 fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const void *O,
                               const void *dO, const float *LSE, void *dQ, void *dK, void *dV,

@@ -283,6 +283,15 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
  * FA_ERR_CUDA if an event could not be read (fa_last_error() says which).
  */
 int fa_num_kernels(void);
+
+/*
+ * Measurement helper for the exponential-rate ceiling of the softmax: runs
+ * one CTA of 1024 threads per SM on the calling thread's current device, each
+ * thread evaluating 8 independent chains of ex2.approx.ftz.f32, and stores the
+ * mean number of ex2 operations per SM clock cycle (from clock64 on each SM)
+ * in *ops_per_clk_per_sm. Synchronises the device; allocates nothing.
+ */
+fa_status fa_measure_exp2_rate(double *ops_per_clk_per_sm);
 const char *fa_kernel_name(int kernel);
 fa_status fa_profile_enable(int enable);
 fa_status fa_profile_collect(float *total_ms, int *launches, int n);

@@ -66,3 +66,10 @@ def test_split_forward_in_a_graph():
     torch.cuda.synchronize()
     assert fa().device_status() == 0
     assert torch.equal(o, o_eager) and torch.equal(lse, lse_eager)
+
+
+def test_exp2_rate_measurement_is_plausible():
+    """The SFU rate probe behind the exponential-rate ceiling: ex2.approx
+    operations per SM clock, between one per SMSP per clock and the FMA rate."""
+    rate = fa().measure_exp2_rate()
+    assert 4.0 <= rate <= 128.0, rate
