@@ -444,25 +444,30 @@ __device__ float g_exp_probe_sink[kMaxProbeBlocks];
 // ex2.approx; thread 0 records the CTA's SM cycles between two block-wide
 // barriers around the loop.
 __global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
+  __syncthreads();
+  // the clock reads are tied to the chains by data dependencies, so the
+  // compiler cannot move the loop out of the timed window
+  long long t0, t1;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+  float zero;
+  asm volatile("{ .reg .s64 z; and.b64 z, %1, 0; cvt.rn.f32.s64 %0, z; }" : "=f"(zero) : "l"(t0));
   float a[kExpProbeChains];
 #pragma unroll
-  for (int c = 0; c < kExpProbeChains; ++c) a[c] = -1e-3f * float(threadIdx.x % 97 + c);
-  __syncthreads();
-  const long long t0 = clock64();
+  for (int c = 0; c < kExpProbeChains; ++c) a[c] = zero - 1e-3f * float(threadIdx.x % 97 + c);
   for (int it = 0; it < kExpProbeIters; ++it) {
 #pragma unroll
     for (int c = 0; c < kExpProbeChains; ++c) {
       float y;
       asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a[c]));
-      a[c] = -y;  // stays in (-1, 0]: no overflow, and a true dependency
+      a[c] = -y;  // stays in [-1, 0): no overflow, and a true dependency
     }
   }
-  __syncthreads();
-  const long long t1 = clock64();
   float s = 0.f;
 #pragma unroll
   for (int c = 0; c < kExpProbeChains; ++c) s += a[c];
-  if (s == 12345.f) g_exp_probe_sink[blockIdx.x] = s;  // keeps the loop alive
+  asm volatile("{ .reg .f32 d; mov.f32 d, %1; mov.u64 %0, %%clock64; }" : "=l"(t1) : "f"(s));
+  if (s == 12345.f) g_exp_probe_sink[blockIdx.x] = s;  // keeps the chains alive
+  __syncthreads();
   if (threadIdx.x == 0 && blockIdx.x < kMaxProbeBlocks)
     g_exp_probe_cycles[blockIdx.x] = (unsigned long long)(t1 - t0);
 }
