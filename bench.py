@@ -402,15 +402,14 @@ def run_cuda(args, dist: Dist):
     # Algorithmic bytes per head: forward reads Q, K, V and writes O (16-bit)
     # and LSE; backward reads Q, K, V, O, dO and LSE, writes dQ, dK, dV, and
     # writes and reads D and LSE*log2(e).
-    exp2_rate = fa.measure_exp2_rate()
+    peak_exps = fa.measure_exp2_rate()  # ex2.approx per second, whole GPU
     sms = props.multi_processor_count
     mhz = clk["sm_mhz"] or peaks.get("sm_max_mhz", 2070.0)
-    peak_exps = exp2_rate * sms * mhz * 1e6
     fwd_exps = fwd_fl / (4.0 * w.d)
     heads = w.B * w.H
     fwd_bytes = heads * ((3 * 2 + 2) * w.N * w.d + 4 * w.N)
     bwd_bytes = heads * ((5 * 2 + 3 * 2) * w.N * w.d + 4 * w.N + 16 * w.N)
-    sfu = {"exp2_ops_per_clk_per_sm": round(exp2_rate, 2),
+    sfu = {"exp2_ops_per_clk_per_sm": round(peak_exps / sms / (mhz * 1e6), 2),
            "peak_exps_per_s": peak_exps,
            "fwd_exps_per_s": fwd_exps / (fwd_ms * 1e-3),
            "fwd_frac": round(fwd_exps / (fwd_ms * 1e-3) / peak_exps, 4),

@@ -277,8 +277,8 @@ def device_status(stream=None) -> int:
 
 
 def measure_exp2_rate() -> float:
-    """ex2.approx operations per SM clock on the current device (a
-    measurement, run once; synchronises)."""
+    """ex2.approx operations per second of the whole current device, at the
+    clocks of the moment (a measurement, run once; synchronises)."""
     r = ctypes.c_double(0.0)
     _check(_lib_fast().fa_measure_exp2_rate(ctypes.byref(r)), "fa_measure_exp2_rate")
     return float(r.value)

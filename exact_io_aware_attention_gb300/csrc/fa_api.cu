@@ -434,26 +434,16 @@ fa_status noalloc_scratch(int dev, void **out) {
 // ---- measurement: the SFU exp2 rate ----------------------------------------
 
 constexpr int kExpProbeThreads = 1024;
-constexpr int kExpProbeIters = 2048;
+constexpr int kExpProbeIters = 4096;
 constexpr int kExpProbeChains = 8;  // independent ex2 chains per thread
-constexpr int kMaxProbeBlocks = 1024;
-__device__ unsigned long long g_exp_probe_cycles[kMaxProbeBlocks];
-__device__ float g_exp_probe_sink[kMaxProbeBlocks];
+__device__ float g_exp_probe_sink;
 
-// One CTA per SM: each thread runs kExpProbeChains independent chains of
-// ex2.approx; thread 0 records the CTA's SM cycles between two block-wide
-// barriers around the loop.
+// One CTA of 1024 threads per SM, each thread running kExpProbeChains
+// independent chains of ex2.approx; the host times the launch with events.
 __global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
-  __syncthreads();
-  // the clock reads are tied to the chains by data dependencies, so the
-  // compiler cannot move the loop out of the timed window
-  long long t0, t1;
-  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
-  float zero;
-  asm volatile("{ .reg .s64 z; and.b64 z, %1, 0; cvt.rn.f32.s64 %0, z; }" : "=f"(zero) : "l"(t0));
   float a[kExpProbeChains];
 #pragma unroll
-  for (int c = 0; c < kExpProbeChains; ++c) a[c] = zero - 1e-3f * float(threadIdx.x % 97 + c);
+  for (int c = 0; c < kExpProbeChains; ++c) a[c] = -1e-3f * float(threadIdx.x % 97 + c);
   for (int it = 0; it < kExpProbeIters; ++it) {
 #pragma unroll
     for (int c = 0; c < kExpProbeChains; ++c) {
@@ -465,11 +455,7 @@ __global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
   float s = 0.f;
 #pragma unroll
   for (int c = 0; c < kExpProbeChains; ++c) s += a[c];
-  asm volatile("{ .reg .f32 d; mov.f32 d, %1; mov.u64 %0, %%clock64; }" : "=l"(t1) : "f"(s));
-  if (s == 12345.f) g_exp_probe_sink[blockIdx.x] = s;  // keeps the chains alive
-  __syncthreads();
-  if (threadIdx.x == 0 && blockIdx.x < kMaxProbeBlocks)
-    g_exp_probe_cycles[blockIdx.x] = (unsigned long long)(t1 - t0);
+  if (s == 12345.f) g_exp_probe_sink = s;  // keeps the chains alive
 }
 
 }  // namespace
@@ -668,23 +654,31 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 
 size_t fa_backward_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
 
-fa_status fa_measure_exp2_rate(double *ops_per_clk_per_sm) {
-  if (!ops_per_clk_per_sm) return FA_ERR_INVALID_ARG;
-  *ops_per_clk_per_sm = 0.0;
+fa_status fa_measure_exp2_rate(double *exps_per_second) {
+  if (!exps_per_second) return FA_ERR_INVALID_ARG;
+  *exps_per_second = 0.0;
   const int sms = sm_count();
-  if (sms <= 0 || sms > kMaxProbeBlocks) return cuda_fail("SM count", cudaErrorInvalidDevice);
-  fa_exp2_probe<<<sms, kExpProbeThreads>>>();
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (sms <= 0) return cuda_fail("SM count", cudaErrorInvalidDevice);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  float ms = 0.f;
+  for (int rep = 0; rep < 2 && e == cudaSuccess; ++rep) {  // the first launch warms up
+    e = cudaEventRecord(e0, 0);
+    if (e == cudaSuccess) {
+      fa_exp2_probe<<<sms, kExpProbeThreads, 0, 0>>>();
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(e1, 0);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
   if (e != cudaSuccess) return cuda_fail("exp2 probe", e);
-  unsigned long long cycles[kMaxProbeBlocks];
-  e = cudaMemcpyFromSymbol(cycles, g_exp_probe_cycles, sizeof(unsigned long long) * sms);
-  if (e != cudaSuccess) return cuda_fail("cudaMemcpyFromSymbol", e);
-  double mean = 0.0;
-  for (int i = 0; i < sms; ++i) mean += (double)cycles[i];
-  mean /= sms;
-  if (mean <= 0.0) return cuda_fail("exp2 probe cycles", cudaErrorUnknown);
-  *ops_per_clk_per_sm = (double)kExpProbeThreads * kExpProbeIters * kExpProbeChains / mean;
+  if (!(ms > 0.f)) return cuda_fail("exp2 probe time", cudaErrorUnknown);
+  *exps_per_second =
+      (double)sms * kExpProbeThreads * kExpProbeIters * kExpProbeChains / (ms * 1e-3);
   return FA_OK;
 }
 

@@ -286,12 +286,13 @@ int fa_num_kernels(void);
 
 /*
  * Measurement helper for the exponential-rate ceiling of the softmax: runs
- * one CTA of 1024 threads per SM on the calling thread's current device, each
- * thread evaluating 8 independent chains of ex2.approx.ftz.f32, and stores the
- * mean number of ex2 operations per SM clock cycle (from clock64 on each SM)
- * in *ops_per_clk_per_sm. Synchronises the device; allocates nothing.
+ * one CTA of 1024 threads per SM on the calling thread's current device (on
+ * the legacy default stream), each thread evaluating 8 independent chains of
+ * ex2.approx.ftz.f32, times the second of two launches with CUDA events, and
+ * stores the ex2 operations per second of the whole GPU, at the clocks of
+ * that moment, in *exps_per_second. Synchronises; allocates no device memory.
  */
-fa_status fa_measure_exp2_rate(double *ops_per_clk_per_sm);
+fa_status fa_measure_exp2_rate(double *exps_per_second);
 const char *fa_kernel_name(int kernel);
 fa_status fa_profile_enable(int enable);
 fa_status fa_profile_collect(float *total_ms, int *launches, int n);
