@@ -440,7 +440,9 @@ __device__ float g_exp_probe_sink;
 
 // One CTA of 1024 threads per SM, each thread running kExpProbeChains
 // independent chains of ex2.approx; the host times the launch with events.
-__global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
+// `key` is a runtime value the sum is compared with, so the compiler cannot
+// prove the chains' results unused.
+__global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe(float key) {
   float a[kExpProbeChains];
 #pragma unroll
   for (int c = 0; c < kExpProbeChains; ++c) a[c] = -1e-3f * float(threadIdx.x % 97 + c);
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(kExpProbeThreads, 1) fa_exp2_probe() {
   float s = 0.f;
 #pragma unroll
   for (int c = 0; c < kExpProbeChains; ++c) s += a[c];
-  if (s == 12345.f) g_exp_probe_sink = s;  // keeps the chains alive
+  if (s == key) g_exp_probe_sink = s;  // keeps the chains alive
 }
 
 }  // namespace
@@ -666,7 +668,7 @@ fa_status fa_measure_exp2_rate(double *exps_per_second) {
   for (int rep = 0; rep < 2 && e == cudaSuccess; ++rep) {  // the first launch warms up
     e = cudaEventRecord(e0, 0);
     if (e == cudaSuccess) {
-      fa_exp2_probe<<<sms, kExpProbeThreads, 0, 0>>>();
+      fa_exp2_probe<<<sms, kExpProbeThreads, 0, 0>>>(1.0e30f);
       e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = cudaEventRecord(e1, 0);
