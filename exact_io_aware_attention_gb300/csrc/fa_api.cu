@@ -110,7 +110,7 @@ fa_status operand_strides(const fa_tensor *t, int B, int H, int rows, int d, int
 // box that runs past `rows` reads zeros there and never the next head; one
 // that runs past column d (d = 96) reads zeros in the missing columns.
 bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, int B, int H,
-                    int rows, int d, bool f16) {
+                    int rows, int d, bool f16, int box_rows = fa::kTile) {
   EncodeTiledFn enc = encoder();
   if (!enc) {
     snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
@@ -119,7 +119,7 @@ bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, 
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)st.n_ * 2, (cuuint64_t)st.h_ * 2,
                                  (cuuint64_t)st.b_ * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)fa::kTile, 1, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t elem[4] = {1, 1, 1, 1};
   const CUresult r =
       enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -280,6 +280,9 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d, f16) ||
       !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d, f16) ||
       !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d, f16))
+    return FA_ERR_CUDA;
+  // O is stored by TMA, one 32-row box per warp
+  if (O->dtype != FA_F32 && !encode_operand(&p.tm_o, O->data, p.so, B, H, Nq, d, f16, 32))
     return FA_ERR_CUDA;
   p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask, f16);
   p.o = O->data;

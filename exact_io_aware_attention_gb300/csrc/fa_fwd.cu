@@ -96,6 +96,52 @@ enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 // (Q, K, V, P and a 16-bit O). D is 64 or 128; a head dimension of 96 runs
 // as 128, the tensor maps reading zeros in columns 96..127, and only the
 // first sh.d columns are stored.
+// Epilogue of one softmax thread for a 16-bit O: its row of O / l (tensor
+// memory -> registers) goes to `s_tile`, this Q tile's buffer, which the MMAs
+// no longer read, in the 128-byte-swizzled layout of the tensor map; then
+// lane 0 stores the warp's 32 rows with TMA (rows past the sequence end are
+// clipped by the map). A function of its own, called once per CTA, so that
+// its registers do not weigh on the softmax loop.
+template <int D, bool kF16>
+__device__ __noinline__ void store_o_rows_tma(const FwdParams &p, uint32_t tO, uint32_t s_tile,
+                                              int r, int tile_row0, float inv_l, bool any,
+                                              int bh) {
+  using L = FwdLayout<D>;
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    if (D == 128 && q * 32 >= p.sh.d) break;  // head dimension 96: columns 96..127 unused
+    uint32_t o[32];
+    if (any) {
+      tmem_ld32(tO + q * 32, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int x = 0; x < 32; ++x) o[x] = 0u;
+    }
+    const uint32_t rowbase = s_tile + (q >> 1) * L::kChunkBytes + r * 128;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t piece = uint32_t((q & 1) * 4 + x) ^ uint32_t(r & 7);
+      st_shared_v4(rowbase + (piece << 4),
+                   pack2<kF16>(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l),
+                   pack2<kF16>(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l),
+                   pack2<kF16>(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l),
+                   pack2<kF16>(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l));
+    }
+  }
+  const int warp_row = r & ~31;                  // this warp's first row in the tile
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((r & 31) == 0 && tile_row0 + warp_row < p.sh.nq) {
+    for (int c = 0; c < L::kChunks; ++c)
+      tma_store_4d(&p.tm_o, s_tile + c * L::kChunkBytes + warp_row * 128, c * 64,
+                   tile_row0 + warp_row, bh % p.sh.heads, bh / p.sh.heads);
+    bulk_commit_group();
+    bulk_wait_group_read0();
+  }
+  __syncwarp();
+}
+
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
@@ -144,6 +190,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    // the Q tiles do not depend on the tile list: load them now, while the
+    // other warps set up
+    if (!(p.debug_flags & kDebugSkipLoads)) {
+      mbar_arrive_expect_tx(bars.q_full(), (has1 ? 2u : 1u) * L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i0 * kTile, h_idx, b_idx,
+                    bars.q_full());
+      if (has1)
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64,
+                      (i0 + 1) * kTile, h_idx, b_idx, bars.q_full());
+    }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -195,17 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
       int pos = 0;
       bool ok = true;
-      const uint32_t qbytes = (has1 ? 2u : 1u) * L::kTileBytes;
-      if (count > 0) {
-        mbar_arrive_expect_tx(bars.q_full(), qbytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i0 * kTile, h_idx, b_idx,
-                      bars.q_full());
-        if (has1)
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_4d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64,
-                        (i0 + 1) * kTile, h_idx, b_idx, bars.q_full());
-      }
       for (int n = 0; n < count && ok; ++n) {
         const int kvrow = entry_j(list[n]) * kTile;
         for (int which = 0; which < 2 && ok; ++which, ++pos) {
@@ -220,8 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                         b_idx, bars.kv_full(s));
         }
       }
-      // teardown: wait (bounded) until every copy this thread issued has landed
-      if (count > 0) mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+      // teardown: wait (bounded) until every copy issued has landed (the Q
+      // tiles were loaded during set-up)
+      mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
       for (int s = 0; s < L::kStages && s < pos; ++s) {
         const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
         mbar_wait(bars.kv_full(s), (last / L::kStages) & 1u, st,
@@ -421,36 +469,41 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const size_t row = to_part ? prow * D : p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
         float *const o32 = to_part ? p.o_part : static_cast<float *>(p.o);
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
+        if (!kSplit && !p.o_f32) {
+          store_o_rows_tma<D, kF16>(p, tO, sQ + t * L::kTileBytes, r, qi * kTile, inv_l, any,
+                                    bh_e);
+        } else {
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
-          uint32_t o[32];
-          if (any) {
-            tmem_ld32(tO + q * 32, o);
-            tmem_wait_ld();
-          } else {
+          for (int q = 0; q < D / 32; ++q) {
+            if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
+            uint32_t o[32];
+            if (any) {
+              tmem_ld32(tO + q * 32, o);
+              tmem_wait_ld();
+            } else {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = 0u;
-          }
-          if (!live) {
-          } else if (to_part || p.o_f32) {
-            float4 *dst = reinterpret_cast<float4 *>(o32 + row + q * 32);
+              for (int x = 0; x < 32; ++x) o[x] = 0u;
+            }
+            if (!live) {
+            } else if (to_part || p.o_f32) {
+              float4 *dst = reinterpret_cast<float4 *>(o32 + row + q * 32);
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(__uint_as_float(o[4 * x]) * inv_l,
-                                   __uint_as_float(o[4 * x + 1]) * inv_l,
-                                   __uint_as_float(o[4 * x + 2]) * inv_l,
-                                   __uint_as_float(o[4 * x + 3]) * inv_l);
-          } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row + q * 32);
+              for (int x = 0; x < 8; ++x)
+                dst[x] = make_float4(__uint_as_float(o[4 * x]) * inv_l,
+                                     __uint_as_float(o[4 * x + 1]) * inv_l,
+                                     __uint_as_float(o[4 * x + 2]) * inv_l,
+                                     __uint_as_float(o[4 * x + 3]) * inv_l);
+            } else {
+              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row + q * 32);
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              uint4 v;
-              v.x = pack2<kF16>(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l);
-              v.y = pack2<kF16>(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l);
-              v.z = pack2<kF16>(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l);
-              v.w = pack2<kF16>(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l);
-              dst[x] = v;
+              for (int x = 0; x < 4; ++x) {
+                uint4 v;
+                v.x = pack2<kF16>(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l);
+                v.y = pack2<kF16>(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l);
+                v.z = pack2<kF16>(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l);
+                v.w = pack2<kF16>(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l);
+                dst[x] = v;
+              }
             }
           }
         }
@@ -458,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (live)
           (to_part ? p.lse_part[prow] : p.lse[(size_t)bh * sh.nq + qrow]) =
               (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+
       }
     }
   }

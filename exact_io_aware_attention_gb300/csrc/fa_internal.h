@@ -70,6 +70,7 @@ struct FwdParams {
   // box 64 x 128 x 1 x 1, 128-byte swizzle; rows past the end of a head and
   // columns past d read zeros
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;                   // map over O (16-bit O only) with a 64 x 32 box, for TMA stores
   Shape sh;
   void *o;                            // 16-bit (the inputs' type) or fp32 rows, strides so
   RowStrides so;

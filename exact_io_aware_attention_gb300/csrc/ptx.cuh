@@ -131,6 +131,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// 4-D tile store from shared memory (a 128-byte-swizzled box) to a map over
+// [B][H][rows][d]; rows past the tensor's extent are not written. Completion
+// is tracked with bulk groups (bulk_commit_group / bulk_wait_group_read).
+__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int x, int y, int z,
+                                             int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until the committed bulk stores of this thread have finished reading
+// shared memory (their global writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // 1-D bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
                                              uint32_t bar) {
