@@ -345,7 +345,10 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   if (!encode_operand(&p.tm_q, Q->data, sq, B, H, Nq, d, f16) ||
       !encode_operand(&p.tm_k, K->data, sk, B, H, Nk, d, f16) ||
       !encode_operand(&p.tm_v, V->data, sv, B, H, Nk, d, f16) ||
-      !encode_operand(&p.tm_do, dO->data, p.sdo, B, H, Nq, d, f16))
+      !encode_operand(&p.tm_do, dO->data, p.sdo, B, H, Nq, d, f16) ||
+      !encode_operand(&p.tm_dq, dQ->data, p.sdq, B, H, Nq, d, f16, 32) ||
+      !encode_operand(&p.tm_dk, dK->data, p.sdk, B, H, Nk, d, f16, 32) ||
+      !encode_operand(&p.tm_dv, dV->data, p.sdv, B, H, Nk, d, f16, 32))
     return FA_ERR_CUDA;
   p.sh = make_shape(B, H, Nq, Nk, d, causal, block_mask, f16);
   p.o = O->data;

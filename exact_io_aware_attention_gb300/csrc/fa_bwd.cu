@@ -47,6 +47,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tile_store.cuh"
 
 namespace fa {
 namespace {
@@ -109,6 +110,25 @@ __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
 // kF16: f16 elements instead of bf16. D is 64 or 128; a head dimension of 96
 // runs as 128 (the tensor maps read zeros in columns 96..127) and only the
 // first sh.d columns of dK and dV are stored.
+// Stage s of the Q_i, dO_i ring, with LSE_i * log2(e) and D_i, onto q_full(s).
+template <int D>
+__device__ __forceinline__ void load_q_stage(const BwdParams &p, const Bars &bars, int s, int i,
+                                             uint32_t s_base, uint32_t sQ, uint32_t sdO,
+                                             size_t stat_head, int h_idx, int b_idx) {
+  using L = DkdvLayout<D>;
+  mbar_arrive_expect_tx(bars.q_full(s), 2 * L::kTileBytes + L::kStatBytes);
+  for (int c = 0; c < L::kChunks; ++c) {
+    tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx,
+                b_idx, bars.q_full(s));
+    tma_load_4d(sdO + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx,
+                b_idx, bars.q_full(s));
+  }
+  const uint32_t sst = s_base + L::kStatOff + s * L::kStatBytes;
+  const size_t srow = stat_head + (size_t)i * kTile;
+  bulk_load_1d(sst, p.lse2 + srow, kTile * 4, bars.q_full(s));
+  bulk_load_1d(sst + kTile * 4, p.delta + srow, kTile * 4, bars.q_full(s));
+}
+
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant__ BwdParams p) {
   using L = DkdvLayout<D>;
@@ -163,6 +183,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
     tma_prefetch_desc(&p.tm_do);
+    // K_j, V_j and the first Q tile's stage depend on blockIdx only: load
+    // them now, while the other warps set up
+    if (any && !(p.debug_flags & kDebugSkipLoads)) {
+      mbar_arrive_expect_tx(bars.kv_full(), 2 * L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_4d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, j * kTile, h_idx, b_idx,
+                    bars.kv_full());
+        tma_load_4d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, j * kTile, h_idx, b_idx,
+                    bars.kv_full());
+      }
+      load_q_stage<D>(p, bars, 0, first, s_base, sQ, sdO, stat_head, h_idx, b_idx);
+    }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -175,31 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
     if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
-      mbar_arrive_expect_tx(bars.kv_full(), 2 * L::kTileBytes);
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, j * kTile, h_idx, b_idx,
-                    bars.kv_full());
-        tma_load_4d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, j * kTile, h_idx, b_idx,
-                    bars.kv_full());
-      }
-      int n = 0;
+      int n = 1;  // K, V and stage 0 (the first Q tile) were loaded during set-up
       bool ok = true;
-      for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
+      for (int i = next_q(sh, first + 1, j); i < T && ok; i = next_q(sh, i + 1, j), ++n) {
         const int s = n & 1;
         const uint32_t u = n >> 1;
         ok = mbar_wait(bars.q_empty(s), (u & 1u) ^ 1u, st, status_code(kKernBwd, kRoleLoad, 1));
         if (!ok) break;
-        mbar_arrive_expect_tx(bars.q_full(s), 2 * L::kTileBytes + L::kStatBytes);
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile,
-                      h_idx, b_idx, bars.q_full(s));
-          tma_load_4d(sdO + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile,
-                      h_idx, b_idx, bars.q_full(s));
-        }
-        const uint32_t sst = s_base + L::kStatOff + s * L::kStatBytes;
-        const size_t srow = stat_head + (size_t)i * kTile;
-        bulk_load_1d(sst, p.lse2 + srow, kTile * 4, bars.q_full(s));
-        bulk_load_1d(sst + kTile * 4, p.delta + srow, kTile * 4, bars.q_full(s));
+        load_q_stage<D>(p, bars, s, i, s_base, sQ, sdO, stat_head, h_idx, b_idx);
       }
       // teardown: every copy issued has landed
       mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleLoad, 2));
@@ -343,34 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     if (ok && any)
       ok = __all_sync(0xffffffffu, mbar_wait(bars.acc_done(), 0, st,
                                              status_code(kKernBwd, kRoleSoftmax, 6)));
-    // tensor-memory loads are warp-wide; rows past the sequence end store nothing
-    const int krow = j * kTile + kr;  // key row within the head
-    const bool live = krow < sh.nk;
+    // dV (warps 4-7) and dK (warps 8-11, times scale) leave through the K and
+    // V buffers, which no MMA reads any more
     if (ok) {
       tc_fence_after();
-      const uint32_t col = h ? L::kColDK : L::kColDV;
-      const float sc = h ? p.scale : 1.f;
-      uint16_t *dst_row = static_cast<uint16_t *>(h ? p.dk : p.dv) +
-                          (h ? p.sdk : p.sdv).row(b_idx, h_idx, krow);
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
-        float v[32];
-        if (any) {
-          ld_cols32(t + col + q * 32, v);
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0.f;
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + q * 32);
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-          if (live)
-            dst[x] = make_uint4(pack2<kF16>(v[8 * x] * sc, v[8 * x + 1] * sc),
-                                pack2<kF16>(v[8 * x + 2] * sc, v[8 * x + 3] * sc),
-                                pack2<kF16>(v[8 * x + 4] * sc, v[8 * x + 5] * sc),
-                                pack2<kF16>(v[8 * x + 6] * sc, v[8 * x + 7] * sc));
-      }
+      store_rows_tma<D, kF16>(h ? &p.tm_dk : &p.tm_dv, t + (h ? L::kColDK : L::kColDV),
+                              h ? sV : sK, kr, j * kTile, 0, h ? p.scale : 1.f, any, sh.d, sh.nk,
+                              h_idx, b_idx);
     }
   }
 

@@ -25,6 +25,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tile_store.cuh"
 
 namespace fa {
 namespace {
@@ -135,6 +136,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
     tma_prefetch_desc(&p.tm_do);
+    // Q_i and dO_i depend on blockIdx only: load them now, while the other
+    // warps set up (the producer waits for them even if the list is empty)
+    if (!(p.debug_flags & kDebugSkipLoads)) {
+      mbar_arrive_expect_tx(bars.q_full(), 2 * L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
+                    bars.q_full());
+        tma_load_4d(sdO + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx, b_idx,
+                    bars.q_full());
+      }
+    }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -161,14 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
 
   if (warp == 0) {
     // ---- TMA producer: Q, dO; then K_0, and per step K_{n+1}, V_n ------------
-    if (elect_one() && count > 0 && !(p.debug_flags & kDebugSkipLoads)) {
-      mbar_arrive_expect_tx(bars.q_full(), 2 * L::kTileBytes);
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
-                    bars.q_full());
-        tma_load_4d(sdO + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx, b_idx,
-                    bars.q_full());
-      }
+    if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
       bool ok = true;
       int nk = 0, nv = 0;  // tiles issued so far
       auto load_k = [&](int n) {
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                       b_idx, bars.v_full(s));
         ++nv;
       };
-      load_k(0);
+      if (count > 0) load_k(0);
       for (int n = 0; n < count && ok; ++n) {
         if (n + 1 < count) load_k(n + 1);
         if (ok) load_v(n);
@@ -351,7 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                                              status_code(kKernBwdDq, kRoleSoftmax, 4)));
     // tensor-memory loads are warp-wide; rows past the sequence end store nothing
     const bool live = qrow < sh.nq;
-    if (ok) {
+    if (ok && D == 128 && count > 0) {
+      // each warpgroup's 64 columns leave through its chunk of the Q buffer,
+      // which no MMA reads any more (count > 0: its Q load has landed; an
+      // empty list stores its zeros directly below)
+      tc_fence_after();
+      store_rows_tma<64, kF16>(&p.tm_dq, t + L::kColDQ + h * 64, sQ + h * L::kChunkBytes, r,
+                               i * kTile, h * 64, p.scale, count > 0, sh.d, sh.nq, h_idx, b_idx);
+    } else if (ok) {
       tc_fence_after();
       constexpr int kHalf = D / 2;
       uint16_t *dst_row =

@@ -40,6 +40,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tile_store.cuh"
 
 namespace fa {
 namespace {
@@ -96,52 +97,6 @@ enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 // (Q, K, V, P and a 16-bit O). D is 64 or 128; a head dimension of 96 runs
 // as 128, the tensor maps reading zeros in columns 96..127, and only the
 // first sh.d columns are stored.
-// Epilogue of one softmax thread for a 16-bit O: its row of O / l (tensor
-// memory -> registers) goes to `s_tile`, this Q tile's buffer, which the MMAs
-// no longer read, in the 128-byte-swizzled layout of the tensor map; then
-// lane 0 stores the warp's 32 rows with TMA (rows past the sequence end are
-// clipped by the map). A function of its own, called once per CTA, so that
-// its registers do not weigh on the softmax loop.
-template <int D, bool kF16>
-__device__ __noinline__ void store_o_rows_tma(const FwdParams &p, uint32_t tO, uint32_t s_tile,
-                                              int r, int tile_row0, float inv_l, bool any,
-                                              int bh) {
-  using L = FwdLayout<D>;
-#pragma unroll
-  for (int q = 0; q < D / 32; ++q) {
-    if (D == 128 && q * 32 >= p.sh.d) break;  // head dimension 96: columns 96..127 unused
-    uint32_t o[32];
-    if (any) {
-      tmem_ld32(tO + q * 32, o);
-      tmem_wait_ld();
-    } else {
-#pragma unroll
-      for (int x = 0; x < 32; ++x) o[x] = 0u;
-    }
-    const uint32_t rowbase = s_tile + (q >> 1) * L::kChunkBytes + r * 128;
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t piece = uint32_t((q & 1) * 4 + x) ^ uint32_t(r & 7);
-      st_shared_v4(rowbase + (piece << 4),
-                   pack2<kF16>(__uint_as_float(o[8 * x + 0]) * inv_l, __uint_as_float(o[8 * x + 1]) * inv_l),
-                   pack2<kF16>(__uint_as_float(o[8 * x + 2]) * inv_l, __uint_as_float(o[8 * x + 3]) * inv_l),
-                   pack2<kF16>(__uint_as_float(o[8 * x + 4]) * inv_l, __uint_as_float(o[8 * x + 5]) * inv_l),
-                   pack2<kF16>(__uint_as_float(o[8 * x + 6]) * inv_l, __uint_as_float(o[8 * x + 7]) * inv_l));
-    }
-  }
-  const int warp_row = r & ~31;                  // this warp's first row in the tile
-  fence_proxy_async_smem();
-  __syncwarp();
-  if ((r & 31) == 0 && tile_row0 + warp_row < p.sh.nq) {
-    for (int c = 0; c < L::kChunks; ++c)
-      tma_store_4d(&p.tm_o, s_tile + c * L::kChunkBytes + warp_row * 128, c * 64,
-                   tile_row0 + warp_row, bh % p.sh.heads, bh / p.sh.heads);
-    bulk_commit_group();
-    bulk_wait_group_read0();
-  }
-  __syncwarp();
-}
-
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
@@ -469,9 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const size_t row = to_part ? prow * D : p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
         float *const o32 = to_part ? p.o_part : static_cast<float *>(p.o);
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
-        if (!kSplit && !p.o_f32) {
-          store_o_rows_tma<D, kF16>(p, tO, sQ + t * L::kTileBytes, r, qi * kTile, inv_l, any,
-                                    bh_e);
+        if (!kSplit && !p.o_f32 && any) {
+          // 16-bit O through this tile's Q buffer, which the MMAs no longer
+          // read (any: its Q load has landed, since the MMAs used it; a tile
+          // without keys stores its zeros directly below)
+          store_rows_tma<D, kF16>(&p.tm_o, tO, sQ + t * L::kTileBytes, r, qi * kTile, 0, inv_l,
+                                  any, sh.d, sh.nq, bh_e % sh.heads, bh_e / sh.heads);
         } else {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {

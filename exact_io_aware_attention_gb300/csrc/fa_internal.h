@@ -89,6 +89,7 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
+  CUtensorMap tm_dq, tm_dk, tm_dv;     // maps over the gradients, 64 x 32 boxes (TMA stores)
   Shape sh;
   const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;
