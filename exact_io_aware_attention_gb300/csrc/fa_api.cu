@@ -12,10 +12,19 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fa.h"
 #include "fa_internal.h"
 
 namespace {
+
+// NVTX range around the work an entry point enqueues (visible in profilers
+// that record NVTX; a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 // Device status word written by kernel-side bounded waits that give up.
 __device__ unsigned int g_status_word = 0u;
@@ -299,6 +308,7 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+  NvtxRange range(n_split > 1 ? "fa_forward (split)" : "fa_forward");
   e = fa::launch_forward(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
 }
@@ -367,6 +377,7 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);
   if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+  NvtxRange range("fa_backward");
   e = fa::launch_backward(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail("backward launch", e);
 }
