@@ -172,13 +172,11 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Shape checks shared by every entry point; `*empty` is set for a no-op call.
-// Head dimension 256 has a forward pass only.
-fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *empty,
-                      bool backward = false) {
+fa_status check_shape(int B, int H, int Nq, int Nk, int d, float scale, bool *empty) {
   *empty = false;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128 && (d != 256 || backward)) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H * Nq == 0) {
     *empty = true;
     return FA_OK;
@@ -325,7 +323,7 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
                         const uint8_t *block_mask, void *workspace, size_t ws_bytes,
                         void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty, true);
+  fa_status s = check_shape(B, H, Nq, Nk, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
@@ -510,6 +508,9 @@ const char *fa_kernel_name(int kind) {
     case fa::kKindBwdDkdv: return "fa_bwd_dkdv";
     case fa::kKindBwdDq: return "fa_bwd_dq";
     case fa::kKindFwdCombine: return "fa_fwd_combine";
+    case fa::kKindBwd256Dv: return "fa_bwd256_dv";
+    case fa::kKindBwd256Dk: return "fa_bwd256_dk";
+    case fa::kKindBwd256Dq: return "fa_bwd256_dq";
     default: return "";
   }
 }
@@ -706,7 +707,7 @@ fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const
                               int B, int H, int N, int d, int causal, float scale,
                               const uint8_t *block_mask, void *stream) {
   bool empty;
-  fa_status s = check_shape(B, H, N, N, d, scale, &empty, true);
+  fa_status s = check_shape(B, H, N, N, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
   const size_t need = fa_backward_workspace_bytes(B, H, N, d);

@@ -22,7 +22,8 @@
 //   fa_bwd_dq_kernel  one CTA per Q tile, looping over its K/V tiles; dQ
 //                     accumulates in tensor memory (fa_bwd_dq.cu)
 // Each gradient is owned by one CTA, so no cross-CTA reduction is needed;
-// the price is that S and dP are recomputed by both kernels.
+// the price is that S and dP are recomputed by both kernels. Head dimension
+// 256 shares fa_bwd_pre and then runs the kernels of fa_bwd_d256.cu.
 //
 // Rows past the end of a sequence (the last, partial Q or K/V tile) arrive
 // as zeros from the tensor maps. A missing query row has LSE * log2(e) = +inf
@@ -430,14 +431,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
 
 template <int D, bool kF16>
 cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
-  using L = DkdvLayout<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv<D, kF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   {
     LaunchProbe probe(kKindBwdPre, stream);
     const unsigned blocks = unsigned(p.sh.tq * kTile / kPreRows) * unsigned(p.sh.bh);
@@ -445,13 +438,25 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  {
-    LaunchProbe probe(kKindBwdDkdv, stream);
-    fa_bwd_dkdv<D, kF16><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
+  if constexpr (D == 256) {
+    return launch_backward_d256(p, stream);  // fa_bwd_d256.cu
+  } else {
+    using L = DkdvLayout<D>;
+    static bool configured = false;
+    if (!configured) {
+      e = cudaFuncSetAttribute(fa_bwd_dkdv<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               L::kBytes);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    {
+      LaunchProbe probe(kKindBwdDkdv, stream);
+      fa_bwd_dkdv<D, kF16><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_backward_dq(p, stream);
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_backward_dq(p, stream);
 }
 
 }  // namespace
@@ -461,6 +466,8 @@ cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
   if (p.sh.d == 64) return f16 ? launch_bwd_d<64, true>(p, stream) : launch_bwd_d<64, false>(p, stream);
   if (p.sh.d == 96 || p.sh.d == 128)
     return f16 ? launch_bwd_d<128, true>(p, stream) : launch_bwd_d<128, false>(p, stream);
+  if (p.sh.d == 256)
+    return f16 ? launch_bwd_d<256, true>(p, stream) : launch_bwd_d<256, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

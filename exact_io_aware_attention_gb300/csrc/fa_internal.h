@@ -107,7 +107,8 @@ struct BwdParams {
 
 // Kernel ids of the measurement hooks (names in fa_kernel_name()).
 enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdDkdv = 2, kKindBwdDq = 3,
-                        kKindFwdCombine = 4, kNumKinds = 5 };
+                        kKindFwdCombine = 4, kKindBwd256Dv = 5, kKindBwd256Dk = 6,
+                        kKindBwd256Dq = 7, kNumKinds = 8 };
 
 // Brackets one launch with CUDA events when measurement is enabled
 // (fa_profile_enable); a no-op otherwise.
@@ -128,9 +129,12 @@ cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);  // + the m
 cudaError_t launch_forward_d256(const FwdParams &p, cudaStream_t stream);  // fa_fwd_d256.cu
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_bwd_dq.cu
+// dV, dK and dQ for head dimension 256, after fa_bwd_pre (fa_bwd_d256.cu)
+cudaError_t launch_backward_d256(const BwdParams &p, cudaStream_t stream);
 
 // Status word codes: 0x80000000 | kernel << 16 | role << 8 | site.
-enum KernelId : uint32_t { kKernFwd = 1, kKernBwdPre = 2, kKernBwd = 3, kKernBwdDq = 4 };
+enum KernelId : uint32_t { kKernFwd = 1, kKernBwdPre = 2, kKernBwd = 3, kKernBwdDq = 4,
+                           kKernBwd256Dv = 5, kKernBwd256Dk = 6, kKernBwd256Dq = 7 };
 __host__ __device__ constexpr uint32_t status_code(uint32_t kernel, uint32_t role, uint32_t site) {
   return 0x80000000u | (kernel << 16) | (role << 8) | site;
 }

@@ -34,8 +34,7 @@
  *    default stream), which must belong to the device that holds Q. Each call
  *    makes that device current on the calling thread. Inputs are only read;
  *    outputs must not overlap one another or an input.
- *  - Supported: d in {64, 96, 128}, and d = 256 for the forward entry points
- *    (the backward returns FA_ERR_UNSUPPORTED for it); 1 <= Nq, Nk <= 65536 (any length: a last,
+ *  - Supported: d in {64, 96, 128, 256}; 1 <= Nq, Nk <= 65536 (any length: a last,
  *    partial tile of 128 rows is handled inside the kernels); B, H >= 1;
  *    B*H*max(Nq, Nk) <= 2^31 - 1; scale finite and > 0. B*H*Nq == 0 is a
  *    no-op that returns FA_OK; Nk == 0 with Nq > 0 is FA_ERR_UNSUPPORTED.
@@ -270,8 +269,9 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 /*
  * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
  * 0 forward, 1 backward preprocess (D_i and LSE*log2 e), 2 backward dK/dV,
- * 3 backward dQ, 4 merge of a split forward; fa_kernel_name() names them
- * ("" for an unknown id).
+ * 3 backward dQ, 4 merge of a split forward, and for head dimension 256 the
+ * backward's 5 dV, 6 dK and 7 dQ kernels; fa_kernel_name() names them ("" for
+ * an unknown id).
  *
  * fa_profile_enable(1): from then on every kernel launch is bracketed by two
  * CUDA events recorded on its stream (no synchronisation, no device memory).

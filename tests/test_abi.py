@@ -231,8 +231,9 @@ def test_split_forward_rejects_bad_arguments(lib):
     assert split_fwd(lib, 1, ws=None, ws_bytes=0) in PASSED_HOST_CHECKS  # no split: no workspace
 
 
-def test_head_dim_256_is_forward_only(lib):
+def test_head_dim_256_passes_host_checks(lib):
     assert fwd_ex(lib, d=256) in PASSED_HOST_CHECKS
-    assert bwd(lib, d=256) == UNSUPPORTED
+    assert bwd(lib, d=256) in PASSED_HOST_CHECKS
     assert lib.fa_backward_noalloc(A, A, A, A, A, A, B_, B_, B_, 1, 1, 256, 256, 0, 0.1, None,
-                                   None) == UNSUPPORTED
+                                   None) in PASSED_HOST_CHECKS
+    assert bwd(lib, d=192) == UNSUPPORTED

@@ -2,7 +2,7 @@
 type, query and key lengths (partial tiles, Nq != Nk), causal mask, block
 mask, key splits and memory layout drawn together, so that combinations the
 targeted tests do not list are covered too. Every output element is checked
-(forward O and LSE; dQ, dK, dV where the backward exists, i.e. d != 256)."""
+(forward O and LSE; dQ, dK, dV)."""
 import numpy as np
 import pytest
 import torch
@@ -71,8 +71,6 @@ def test_random_configuration(seed):
     rounded = torch.from_numpy(o_ref).to(c["dtype"]).double().numpy()
     r, r_floor = rel_l2(f64(o), o_ref), rel_l2(rounded, o_ref)
     assert np.sqrt(max(0.0, r * r - r_floor * r_floor)) <= 2e-3, what
-    if d == 256:
-        return
     g = oracle.backward(*x, causal=c["causal"], scale=scale, block_mask=mk)
     dq, dk, dv = fa().backward(q, k, v, o, do, lse, causal=c["causal"], block_mask=m)
     torch.cuda.synchronize()
