@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t sQ = s_base + L::kQOff;
   const uint32_t sKV = s_base + L::kKVOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort [3] ring positions loaded in set-up
   Bars bars{s_base + L::kBarOff, L::kStages};
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
@@ -157,6 +157,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tma_load_4d(sQ + L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64,
                       (i0 + 1) * kTile, h_idx, b_idx, bars.q_full());
     }
+    // and the first K/V tile of the list (the smallest key tile either Q
+    // tile sees) into ring positions 0 and 1; a split CTA starts further
+    // into the list, which is known only after the list is built
+    int pre = 0;
+    if constexpr (!kSplit) {
+      const int jmax0 = sh.last_kv_tile(i0);
+      const int jmax1 = has1 ? sh.last_kv_tile(i0 + 1) : -1;
+      int j0 = -1;
+      for (int j = 0; j <= max(jmax0, jmax1) && j0 < 0; ++j)
+        if ((j <= jmax0 && sh.mask_allows(i0, j)) || (j <= jmax1 && sh.mask_allows(i0 + 1, j)))
+          j0 = j;
+      if (j0 >= 0 && !(p.debug_flags & kDebugSkipLoads)) {
+        for (int which = 0; which < 2; ++which) {
+          mbar_arrive_expect_tx(bars.kv_full(which), L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(sKV + which * L::kTileBytes + c * L::kChunkBytes,
+                        which ? &p.tm_v : &p.tm_k, c * 64, j0 * kTile, h_idx, b_idx,
+                        bars.kv_full(which));
+        }
+        pre = 2;
+      }
+    }
+    misc[3] = pre;  // ring positions already issued
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -206,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
     if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
-      int pos = 0;
+      int pos = misc[3];  // K and V of list[0] may have been issued during set-up
       bool ok = true;
-      for (int n = 0; n < count && ok; ++n) {
+      for (int n = pos / 2; n < count && ok; ++n) {
         const int kvrow = entry_j(list[n]) * kTile;
         for (int which = 0; which < 2 && ok; ++which, ++pos) {
           const int s = pos % L::kStages;

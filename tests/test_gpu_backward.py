@@ -65,30 +65,34 @@ def test_backward_block_sparse_small(causal, d):
     assert (dk[:, :, 768:896] == 0).all() and (dv[:, :, 768:896] == 0).all()
 
 
-def test_backward_peaked_softmax():
-    """Score std ~16 (q, k doubled, scale 0.5): rows are nearly one-hot. D_i is
-    formed from the stored bf16 O (D_i = dO_i . O_i), and its rounding error
-    (~2^-9 |dO_i||O_i| / sqrt(3)) does not shrink while dP_ij - D_i for the
-    dominant key does, so dS loses relative accuracy there. dV does not use D
-    and keeps the standard tolerance; dQ and dK are held to 2e-2."""
-    inp = gen.make_inputs(1, 2, 512, 64, case=600)
+@pytest.mark.parametrize("d,scale", [(64, 0.5), (256, 0.25)])
+def test_backward_peaked_softmax(d, scale):
+    """Score std ~16 (q, k doubled, scale 0.5 at d = 64, 0.25 at d = 256):
+    rows are nearly one-hot. D_i is formed from the stored bf16 O
+    (D_i = dO_i . O_i), and its rounding error (~2^-9 |dO_i||O_i| / sqrt(3))
+    does not shrink while dP_ij - D_i for the dominant key does, so dS loses
+    relative accuracy there. dV does not use D and keeps the standard
+    tolerance; dQ and dK are held to 2e-2."""
+    inp = gen.make_inputs(1, 2, 512, d, case=600)
     for t in ("q", "k"):
         inp[t] = (inp[t].float() * 2).to(torch.bfloat16)
-    g = oracle.backward(*(f64(inp[t]) for t in ("q", "k", "v", "do")), scale=0.5)
-    dq, dk, dv = run_fwd_bwd(inp, False, 0.5, None)
+    g = oracle.backward(*(f64(inp[t]) for t in ("q", "k", "v", "do")), scale=scale)
+    dq, dk, dv = run_fwd_bwd(inp, False, scale, None)
     check_grad(f64(dv), g["dv"], "dv", "peaked")
     for name, x in (("dq", dq), ("dk", dk)):
         r = rel_l2(f64(x), g[name])
         assert r <= 2e-2, f"peaked {name} rel_l2={r:.3e}"
 
 
-def test_backward_repeatable_within_tolerance():
-    """dQ is accumulated with fp32 atomics (order varies); dK and dV are not."""
-    inp = gen.make_inputs(2, 2, 1024, 128, case=601)
+@pytest.mark.parametrize("d", [128, 256])
+def test_backward_is_deterministic(d):
+    """Every gradient tile is owned and written by one CTA in a fixed order
+    (no atomics), so repeated calls give bitwise-identical dQ, dK and dV."""
+    inp = gen.make_inputs(2, 2, 1024, d, case=601)
     a = run_fwd_bwd(inp, True, None, None)
     b = run_fwd_bwd(inp, True, None, None)
-    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
-    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
 
 
 def test_autograd_wrapper_matches_backward():
