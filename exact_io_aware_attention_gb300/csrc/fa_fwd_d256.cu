@@ -12,6 +12,7 @@
 //   warp 0      TMA producer: Q once (4 boxes of 64 columns), then K_j and
 //               V_j as 128-column halves through a ring of 5 32 KB slots, in
 //               the order the MMAs consume them: K_0, K_1, V_0, K_2, V_1, ...
+//               (Q and K_0 are issued during set-up, before the CTA barrier)
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
 //   warp 2      builds the list of K/V tiles to visit
 //   warps 4-7   softmax, thread = query row = TMEM lane
@@ -20,10 +21,12 @@
 // buffer. MMA order: S(0), S(1), then per tile n: PV(n), S(n+2); the tensor
 // core computes S(n+1) while the softmax of tile n runs, and S(n+2) is issued
 // after PV(n) has been issued, so it overwrites P(n) only after PV(n) read it.
+// A 16-bit O leaves through the Q buffer with TMA stores (tile_store.cuh).
 #include <math.h>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tile_store.cuh"
 
 namespace fa {
 namespace {
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
   const uint32_t sQ = s_base + L::kQOff;
   const uint32_t sRing = s_base + L::kRingOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort [3] loads in set-up
   Bars bars{s_base + L::kBarOff};
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
@@ -117,6 +120,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    // Q and the first K tile of the list (the smallest key tile this Q tile
+    // sees) do not depend on the list: load them now, while the other warps
+    // set up. A split CTA starts further into the list, known only later.
+    int pre = 0;
+    if constexpr (!kSplit) {
+      const int jmax = sh.last_kv_tile(i);
+      int j0 = -1;
+      for (int j = 0; j <= jmax && j0 < 0; ++j)
+        if (sh.mask_allows(i, j)) j0 = j;
+      if (j0 >= 0 && !(p.debug_flags & kDebugSkipLoads)) {
+        mbar_arrive_expect_tx(bars.q_full(), L::kQBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
+                      bars.q_full());
+        for (int h = 0; h < 2; ++h) {  // ring positions 0 and 1: K_{j0}, both halves
+          mbar_arrive_expect_tx(bars.full(h), L::kSlotBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sRing + h * L::kSlotBytes + c * L::kChunkBytes, &p.tm_k, h * 128 + c * 64,
+                        j0 * kTile, h_idx, b_idx, bars.full(h));
+        }
+        pre = 2;
+      }
+    }
+    misc[3] = pre;  // ring positions (and Q) already issued
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -159,12 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
     if (elect_one() && count > 0 && !(p.debug_flags & kDebugSkipLoads)) {
-      mbar_arrive_expect_tx(bars.q_full(), L::kQBytes);
-      for (int c = 0; c < 4; ++c)
-        tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
-                    bars.q_full());
+      const int pre = misc[3];
+      if (pre == 0) {
+        mbar_arrive_expect_tx(bars.q_full(), L::kQBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sQ + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx, b_idx,
+                      bars.q_full());
+      }
       bool ok = true;
-      int issued = 0;  // == the ring position of the next load
+      int issued = pre;  // == the ring position of the next load
       // one half (h) of K_j or V_j into the next ring slot
       auto load_half = [&](const CUtensorMap *tm, int j, int h) {
         const int s = issued % L::kSlots;
@@ -178,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
                       h_idx, b_idx, bars.full(s));
         ++issued;
       };
-      for (int h = 0; h < 2 && ok; ++h) load_half(&p.tm_k, 0, h);
+      for (int h = pre; h < 2 && ok; ++h) load_half(&p.tm_k, 0, h);
       for (int n = 0; n < count && ok; ++n) {
         for (int h = 0; h < 2 && ok && n + 1 < count; ++h) load_half(&p.tm_k, n + 1, h);
         for (int h = 0; h < 2 && ok; ++h) load_half(&p.tm_v, n, h);
@@ -352,8 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
       const size_t row = kSplit ? prow * D : p.so.row(b_idx, h_idx, qrow);
       float *const o32 = kSplit ? p.o_part : static_cast<float *>(p.o);
       const float inv_l = (count > 0 && l > 0.f) ? 1.f / l : 0.f;
+      // a 16-bit O leaves through the Q buffer (no MMA reads it any more;
+      // count > 0: its load has landed) with TMA stores
+      const bool via_tma = !kSplit && !p.o_f32 && count > 0;
+      if (via_tma)
+        store_rows_tma<D, kF16>(&p.tm_o, tO, sQ, r, i * kTile, 0, inv_l, true, sh.d, sh.nq, h_idx,
+                                b_idx);
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
+      for (int q = 0; q < D / 32 && !via_tma; ++q) {
         uint32_t o[32];
         if (count > 0) {
           tmem_ld32(tO + q * 32, o);
