@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
   using L = DvLayout;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort [3] loads in set-up
   // the 128-byte swizzle needs 1024-byte aligned tiles; the layout has no
   // room for alignment slack, so a misaligned base is reported
   if (s_base & 1023u) {
@@ -211,12 +211,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_do);
-    // K_j depends on blockIdx only: load it now, while the other warps set up
+    // K_j and the operands of the first two S^T (LSE log2e, both Q halves)
+    // depend on blockIdx only: load them now, while the other warps set up
+    int pre = 0;
     if (any && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.k_full(), kTileBytes);
       for (int c = 0; c < 4; ++c)
         tma_load_4d(sK + c * kChunkBytes, &p.tm_k, c * 64, j * kTile, h_idx, b_idx, bars.k_full());
+      for (int i = first; i < T && pre < 2; i = next_q(sh, i + 1, j), ++pre) {
+        mbar_arrive_expect_tx(bars.stat_full(pre), L::kStatBytes);
+        bulk_load_1d(s_base + L::kStatOff + pre * L::kStatBytes, p.lse2 + stat_head + (size_t)i * kTile,
+                     L::kStatBytes, bars.stat_full(pre));
+        for (int h = 0; h < 2; ++h) {  // ring positions 2 pre + h
+          mbar_arrive_expect_tx(bars.full(2 * pre + h), kHalfBytes);
+          load_half(sRing + (2 * pre + h) * kHalfBytes, &p.tm_q, h, i * kTile, h_idx, b_idx,
+                    bars.full(2 * pre + h));
+        }
+      }
     }
+    misc[3] = pre;  // S^T steps whose operands were issued during set-up
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -242,8 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
         load_half(sRing + s * kHalfBytes, tm, h, i * kTile, h_idx, b_idx, bars.full(s));
         ++issued;
       };
-      // step nst's LSE log2e, then both halves of Q_i
+      // step nst's LSE log2e, then both halves of Q_i (already issued during
+      // set-up for the first misc[3] steps)
+      const int pre = misc[3];
       auto load_x = [&](int i) {
+        if (nst < pre) {
+          ++nst;
+          issued += 2;
+          return;
+        }
         const int b = nst & 1;
         ok = ok && mbar_wait(bars.stat_empty(b), ((nst >> 1) & 1u) ^ 1u, st,
                              status_code(kKernBwd256Dv, kRoleLoad, 2));
@@ -469,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
   constexpr uint32_t kKern = kKeys ? kKernBwd256Dk : kKernBwd256Dq;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort [3] loads in set-up
   if (s_base & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
     if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, status_code(kKern, kRoleInit, 1));
     return;
@@ -529,14 +549,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
     tma_prefetch_desc(tm_a2);
     tma_prefetch_desc(tm_b1);
     tma_prefetch_desc(tm_b2);
-    // A1 and A2 depend on blockIdx only: load them now
+    // A1, A2 and the first ring positions (both halves of B1 and the first
+    // half of B2 of the first column tile, with its statistics) depend on
+    // blockIdx only: load them now
+    int pre = 0;
     if (any && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.a_full(), 2 * kTileBytes);
       for (int c = 0; c < 4; ++c) {
         tma_load_4d(sA1 + c * kChunkBytes, tm_a1, c * 64, rt * kTile, h_idx, b_idx, bars.a_full());
         tma_load_4d(sA2 + c * kChunkBytes, tm_a2, c * 64, rt * kTile, h_idx, b_idx, bars.a_full());
       }
+      if constexpr (kKeys) {
+        const uint32_t dst = s_base + L::kStatOff;
+        const size_t row = stat_head + (size_t)first * kTile;
+        mbar_arrive_expect_tx(bars.stat_full(0), L::kStatBytes);
+        bulk_load_1d(dst, p.lse2 + row, kTile * 4, bars.stat_full(0));
+        bulk_load_1d(dst + kTile * 4, p.delta + row, kTile * 4, bars.stat_full(0));
+      }
+      for (int q = 0; q < L::kSlots; ++q) {  // positions 0, 1: B1 halves; 2: B2 half 0
+        mbar_arrive_expect_tx(bars.full(q), kHalfBytes);
+        load_half(sRing + q * kHalfBytes, q < 2 ? tm_b1 : tm_b2, q & 1, first * kTile, h_idx, b_idx,
+                  bars.full(q));
+      }
+      pre = L::kSlots;
     }
+    misc[3] = pre;  // ring positions issued during set-up
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -551,8 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
     if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
       bool ok = true;
       int issued = 0, nst = 0;
+      const int pre = misc[3];  // positions (and the first statistics) issued in set-up
       auto ring_load = [&](const CUtensorMap *tm, int x) {
         for (int h = 0; h < 2 && ok; ++h) {
+          if (issued < pre) {
+            ++issued;
+            continue;
+          }
           const int s = issued % L::kSlots;
           ok = mbar_wait(bars.empty(s), ((issued / L::kSlots) & 1u) ^ 1u, st,
                          status_code(kKern, kRoleLoad, 1));
@@ -565,6 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
       // dK: LSE_i log2e and D_i of step nst (Q tile i)
       auto load_stats = [&](int i) {
         if constexpr (kKeys) {
+          if (nst == 0 && pre > 0) {
+            nst = 1;
+            return;
+          }
           const int b = nst & 1;
           ok = ok && mbar_wait(bars.stat_empty(b), ((nst >> 1) & 1u) ^ 1u, st,
                                status_code(kKern, kRoleLoad, 2));
