@@ -12,15 +12,19 @@
 // boundary get P = 0 on the tiles that need it.
 //
 // 12 warps:
-//   warp 0      TMA producer: Q_i and dO_i once; K_j (3-slot ring), V_j (2 slots)
+//   warp 0      TMA producer: Q_i and dO_i once; K_j (3-slot ring) and V_j
+//               (2 slots), interleaved
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
 //   warp 2      builds the list of K/V tiles to visit
 //   warps 4-7   thread = query row; keys 0..63 of each tile
 //   warps 8-11  thread = query row; keys 64..127 of each tile
-// Tensor memory: [0,128) S_ij, [128,256) dP_ij, [256,320) dS_ij as packed
-// 16-bit pairs (the A operand of the dQ MMA), [384,384+d) dQ accumulator.
-// MMA order per step n: S(n+1) once S(n) has been read, dQ += dS(n) K_n once
-// dS(n) is in tensor memory, then dP(n+1).
+// Tensor memory: [0,128) S_ij, [128,256) dP_ij, [256,384) dS_ij as packed
+// 16-bit pairs in two buffers of 64 columns (the A operand of the dQ MMA;
+// step n uses buffer n & 1), [384,384+d) dQ accumulator. MMA order per step
+// n: S(n+1) once S(n) has been read, dP(n+1) once dP(n) has been read, then
+// dQ += dS(n) K_n once dS(n) is in tensor memory, so that the tensor core
+// computes S(n+1) and dP(n+1) while P and dS of step n are formed; with two
+// dS buffers dS(n+1) does not wait for dQ(n).
 #include <math.h>
 
 #include "fa_internal.h"
@@ -45,8 +49,8 @@ struct DqLayout {
   static constexpr int kListOff = kVOff + kVSlots * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
   // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free,
-  // dp_full, ds_full, dq_step, dq_final, teardown
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 7;
+  // dp_full, ds_full[2], dq_step[2], dq_final, teardown, dp_free
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -63,10 +67,11 @@ struct Bars {
   __device__ uint32_t s_full() const { return base + 8 * 11; }
   __device__ uint32_t s_free() const { return base + 8 * 12; }
   __device__ uint32_t dp_full() const { return base + 8 * 13; }
-  __device__ uint32_t ds_full() const { return base + 8 * 14; }
-  __device__ uint32_t dq_step() const { return base + 8 * 15; }
+  __device__ uint32_t ds_full(int b) const { return base + 8 * (b ? 18 : 14); }
+  __device__ uint32_t dq_step(int b) const { return base + 8 * (b ? 19 : 15); }
   __device__ uint32_t dq_final() const { return base + 8 * 16; }
   __device__ uint32_t teardown() const { return base + 8 * 17; }
+  __device__ uint32_t dp_free() const { return base + 8 * 20; }
 };
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
@@ -126,8 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_free(), 256);
     mbar_init(bars.dp_full(), 1);
-    mbar_init(bars.ds_full(), 256);
-    mbar_init(bars.dq_step(), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.ds_full(b), 256);
+      mbar_init(bars.dq_step(b), 1);
+    }
+    mbar_init(bars.dp_free(), 256);
     mbar_init(bars.dq_final(), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
@@ -200,9 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                       b_idx, bars.v_full(s));
         ++nv;
       };
-      if (count > 0) load_k(0);
+      // K_j and V_j in the order the MMAs consume them: S(n+1) and dP(n+1)
+      // are issued before dQ(n), so V_{n+1} must not wait behind K_{n+2}
       for (int n = 0; n < count && ok; ++n) {
-        if (n + 1 < count) load_k(n + 1);
+        load_k(n);
         if (ok) load_v(n);
       }
       // teardown: every copy issued has landed
@@ -260,29 +269,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
           issue_sq(sQ, sK + ks1 * L::kTileBytes, L::kColS);
           mma_commit(bars.s_full());
         }
-        // dQ += dS(n) K_n: A = dS from tensor memory (8 columns per 16 keys),
-        // B = K_n with keys as K (MN-major, 16 key rows per step)
-        ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwdDq, kRoleMma, 6));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sK + ks * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16kind_ts(tmem + L::kColDQ, tmem + L::kColDS + kk * 8,
-                      sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024), kIdDq,
-                      (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bars.dq_step());
-        mma_commit(bars.k_empty(ks));
         if (n + 1 < count) {
           const int vs = (n + 1) % L::kVSlots;
-          ok = mbar_wait(bars.v_full(vs), ((n + 1) / L::kVSlots) & 1, st,
-                         status_code(kKernBwdDq, kRoleMma, 7));
+          ok = mbar_wait(bars.dp_free(), n & 1, st, status_code(kKernBwdDq, kRoleMma, 9));
+          if (ok) ok = mbar_wait(bars.v_full(vs), ((n + 1) / L::kVSlots) & 1, st,
+                                 status_code(kKernBwdDq, kRoleMma, 7));
           if (!ok) break;
           tc_fence_after();
           issue_sq(sdO, sV + vs * L::kTileBytes, L::kColDP);
           mma_commit(bars.dp_full());
           mma_commit(bars.v_empty(vs));
         }
+        const int b = n & 1;
+        ok = mbar_wait(bars.ds_full(b), (n >> 1) & 1, st, status_code(kKernBwdDq, kRoleMma, 6));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sK + ks * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_f16kind_ts(tmem + L::kColDQ, tmem + L::kColDS + 64 * b + kk * 8,
+                      sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024), kIdDq,
+                      (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bars.dq_step(b));
+        mma_commit(bars.k_empty(ks));
       }
       if (ok && count > 0) mma_commit(bars.dq_final());
       mma_commit(bars.teardown());
@@ -333,22 +342,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       for (int q = 0; q < 2; ++q) {
         float dp[32];
         ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
+        if (q == 1) {
+          tc_fence_before();
+          mbar_arrive(bars.dp_free());
+        }
 #pragma unroll
         for (int x = 0; x < 32; x += 2)
           dsp[16 * q + x / 2] = pack2<kF16>(pr[32 * q + x] * (dp[x] - dd),
                                             pr[32 * q + x + 1] * (dp[x + 1] - dd));
       }
-      // the dS columns are free once the previous dQ MMA has read them
-      if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_step(), (n - 1) & 1, st,
+      const int b = n & 1;
+      if (n >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_step(b), ((n >> 1) + 1) & 1, st,
                                                status_code(kKernBwdDq, kRoleSoftmax, 3)));
         if (!ok) break;
         tc_fence_after();
       }
-      tmem_st32(t + L::kColDS + 32 * h, dsp);
+      tmem_st32(t + L::kColDS + 64 * b + 32 * h, dsp);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bars.ds_full());
+      mbar_arrive(bars.ds_full(b));
     }
     // epilogue: dQ = scale * accumulator, this half of the d columns
     if (ok && count > 0)
