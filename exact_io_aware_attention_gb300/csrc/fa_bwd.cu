@@ -67,7 +67,7 @@ struct DkdvLayout {
   static constexpr int kStatOff = kdOOff + 2 * kTileBytes; // [2 stages][lse2 128 | delta 128] fp32
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kBarOff = kStatOff + 2 * kStatBytes;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 15;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -85,6 +85,7 @@ struct Bars {
   __device__ uint32_t ds_full() const { return base + 8 * 9; }
   __device__ uint32_t acc_done() const { return base + 8 * 11; }
   __device__ uint32_t teardown() const { return base + 8 * 12; }
+  __device__ uint32_t dv_done() const { return base + 8 * 13; }
 };
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     mbar_init(bars.ds_full(), 256);
     mbar_init(bars.acc_done(), 1);
     mbar_init(bars.teardown(), 1);
+    mbar_init(bars.dv_done(), 1);
     misc[2] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q);
@@ -267,6 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         if (!ok) break;
         tc_fence_after();
         issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0);
+        // dV is final after the last step's dV MMA: its epilogue need not
+        // wait for the last dK
+        if (inext >= T) mma_commit(bars.dv_done());
         if (inext < T) {
           ok = mbar_wait(bars.q_full(s1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 4));
           if (!ok) break;
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     }
     // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled)
     if (ok && any)
-      ok = __all_sync(0xffffffffu, mbar_wait(bars.acc_done(), 0, st,
+      ok = __all_sync(0xffffffffu, mbar_wait(h ? bars.acc_done() : bars.dv_done(), 0, st,
                                              status_code(kKernBwd, kRoleSoftmax, 6)));
     // dV (warps 4-7) and dK (warps 8-11, times scale) leave through the K and
     // V buffers, which no MMA reads any more

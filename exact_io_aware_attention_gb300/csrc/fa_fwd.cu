@@ -58,10 +58,10 @@ struct FwdLayout {
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
   static constexpr int kListOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, teardown
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], teardown
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kBytes = kMiscOff + 32;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
   static_assert(kAlloc <= 232448, "shared memory budget");
   // P_t (16-bit pairs, 64 columns) lives in tensor memory as the A operand of
@@ -79,8 +79,8 @@ struct Bars {
   __device__ uint32_t kv_empty(int s) const { return base + 8 * (1 + stages + s); }
   __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 2 * stages + t); }
   __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 2 * stages + t); }
-  __device__ uint32_t o_done() const { return base + 8 * (5 + 2 * stages); }
-  __device__ uint32_t teardown() const { return base + 8 * (6 + 2 * stages); }
+  __device__ uint32_t o_done(int t) const { return base + 8 * (5 + 2 * stages + t); }
+  __device__ uint32_t teardown() const { return base + 8 * (7 + 2 * stages); }
 };
 
 // list entry: bits 0-11 key tile j; bits 12/13: Q tile 0/1 needs element-wise
@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t sQ = s_base + L::kQOff;
   const uint32_t sKV = s_base + L::kKVOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem base [1] count [2] abort [3] ring positions loaded in set-up
+  // [0] tmem base [1] count [2] abort [3] ring positions loaded in set-up
+  // [4], [5] last list entry of Q tile 0 / 1
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
   Bars bars{s_base + L::kBarOff, L::kStages};
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bars.s_full(t), 1);
       mbar_init(bars.p_full(t), 128);
     }
-    mbar_init(bars.o_done(), 1);
+    for (int t = 0; t < 2; ++t) mbar_init(bars.o_done(t), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
     fence_mbar_init();
@@ -218,7 +220,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       count = hi - lo;
     }
-    if (lane == 0) misc[1] = count;
+    // the last entry each Q tile is active in (-1: none)
+    __syncwarp();
+    int last0 = -1, last1 = -1;
+    for (int base = 0; base < count; base += 32) {
+      const int n = base + lane;
+      if (n < count) {
+        const uint32_t e = list[n];
+        if (entry_act(e, 0)) last0 = n;
+        if (entry_act(e, 1)) last1 = n;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      last0 = max(last0, __shfl_xor_sync(0xffffffffu, last0, off));
+      last1 = max(last1, __shfl_xor_sync(0xffffffffu, last1, off));
+    }
+    if (lane == 0) {
+      misc[1] = count;
+      misc[4] = last0;
+      misc[5] = last1;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -263,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       bool ok = count == 0 || mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
       uint32_t pcount[2] = {0, 0};
       bool first_pv[2] = {true, true};
+      // misc[4 + t]: the last list entry Q tile t is active in (from warp 2)
 
       auto issue_s = [&](int t, int kslot) {
         const uint32_t q_base = sQ + t * L::kTileBytes;
@@ -323,6 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tc_fence_after();
             issue_pv(t, vslot, first_pv[t]);
             first_pv[t] = false;
+            // O_t is final once this entry's PV has completed: under causal
+            // masking Q tile 0 usually ends one K/V tile before Q tile 1, and
+            // its epilogue then overlaps tile 1's last step
+            if (n == *reinterpret_cast<volatile int *>(&misc[4 + t])) mma_commit(bars.o_done(t));
           }
           if (has_next && entry_act(en, t)) {
             issue_s(t, kslot);
@@ -333,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         mma_commit(bars.kv_empty(vslot));
         if (has_next) mma_commit(bars.kv_empty(kslot));
       }
-      if (ok && count > 0) mma_commit(bars.o_done());
       // teardown: every MMA this thread issued has completed
       mma_commit(bars.teardown());
       mbar_wait(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
@@ -432,7 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       // epilogue: O / l and LSE
       if (ok && any)
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.o_done(), 0, st,
+        // this warpgroup's o_done(t), its address from threadIdx (an address
+        // computed from t here costs the softmax loop registers and spills)
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.o_done(0) + ((~threadIdx.x & 128u) >> 4), 0, st,
                                                status_code(kKernFwd, kRoleSoftmax, 3)));
       // tensor-memory loads are warp-wide; rows past the sequence end store nothing
       const int qrow = qi * kTile + r;  // query row within the head
