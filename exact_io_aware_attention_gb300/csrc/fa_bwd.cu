@@ -34,6 +34,7 @@
 //   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per step (2 stages)
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
 //   warps 4-7   thread = key row: P^T and dS^T for queries 0..63; then dV out
+//               (once the last dV MMA has completed: dv_done)
 //   warps 8-11  thread = key row: P^T and dS^T for queries 64..127; then dK out
 // Tensor memory (512 columns): [0,128) S^T, [128,256) dP^T, then dV and dK
 // (d columns each). P^T and dS^T (16-bit pairs) are the tensor-memory A
