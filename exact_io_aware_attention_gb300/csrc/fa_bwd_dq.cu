@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   using L = DqLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
-  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [1] count [2] abort
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [1] count [2] abort [3] set-up loads
   if (s_base & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
     if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, status_code(kKernBwdDq, kRoleInit, 1));
     return;
@@ -145,7 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     tma_prefetch_desc(&p.tm_v);
     tma_prefetch_desc(&p.tm_do);
     // Q_i and dO_i depend on blockIdx only: load them now, while the other
-    // warps set up (the producer waits for them even if the list is empty)
+    // warps set up (the producer waits for them even if the list is empty);
+    // so do K and V of the first list entry (the smallest visible key tile),
+    // into K slot 0 and V slot 0
+    int pre = 0;
     if (!(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.q_full(), 2 * L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c) {
@@ -154,7 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         tma_load_4d(sdO + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx, b_idx,
                     bars.q_full());
       }
+      const int jmax = sh.last_kv_tile(i);
+      int j0 = -1;
+      for (int j = 0; j <= jmax && j0 < 0; ++j)
+        if (sh.mask_allows(i, j)) j0 = j;
+      if (j0 >= 0) {
+        mbar_arrive_expect_tx(bars.k_full(0), L::kTileBytes);
+        mbar_arrive_expect_tx(bars.v_full(0), L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_4d(sK + c * L::kChunkBytes, &p.tm_k, c * 64, j0 * kTile, h_idx, b_idx,
+                      bars.k_full(0));
+          tma_load_4d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, j0 * kTile, h_idx, b_idx,
+                      bars.v_full(0));
+        }
+        pre = 1;
+      }
     }
+    misc[3] = pre;  // list entries whose K and V were loaded during set-up
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
     tmem_relinquish();
@@ -183,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     // ---- TMA producer: Q, dO; then K_0, and per step K_{n+1}, V_n ------------
     if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
       bool ok = true;
-      int nk = 0, nv = 0;  // tiles issued so far
+      const int pre = misc[3];
+      int nk = pre, nv = pre;  // tiles issued so far (entry 0's K and V may be in already)
       auto load_k = [&](int n) {
         const int s = n % L::kKSlots;
         const uint32_t u = n / L::kKSlots;
@@ -210,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       };
       // K_j and V_j in the order the MMAs consume them: S(n+1) and dP(n+1)
       // are issued before dQ(n), so V_{n+1} must not wait behind K_{n+2}
-      for (int n = 0; n < count && ok; ++n) {
+      for (int n = pre; n < count && ok; ++n) {
         load_k(n);
         if (ok) load_v(n);
       }
