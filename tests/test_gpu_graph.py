@@ -16,8 +16,9 @@ def fa():
     return m
 
 
-def test_forward_backward_graph_replays_match_eager():
-    B, H, N, d = 2, 4, 1000, 128
+@pytest.mark.parametrize("d", [128, 256])
+def test_forward_backward_graph_replays_match_eager(d):
+    B, H, N = 2, 4, 1000
     first = gen.make_inputs(B, H, N, d, case=990)
     q, k, v, do = (first[t].cuda() for t in ("q", "k", "v", "do"))
     o = torch.empty_like(q)

@@ -46,7 +46,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
 @pytest.mark.gpu
 def test_noalloc_backward_matches_workspace_backward(lib):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    cases = [((1, 4, 1024, 128), True, None), ((2, 2, 768, 64), False, 0.2)]
+    cases = [((1, 4, 1024, 128), True, None), ((2, 2, 768, 64), False, 0.2),
+             ((1, 2, 700, 256), True, None)]
     for n, (shape, causal, scale) in enumerate(cases):
         B, H, N, d = shape
         assert lib.fa_backward_workspace_bytes(B, H, N, d) <= lib.fa_backward_noalloc_max_bytes()
