@@ -58,7 +58,7 @@ constexpr int kThreads = 384;
 
 template <int D>
 struct DkdvLayout {
-  static constexpr int kChunks = D / 64;
+  static constexpr int kChunks = (D + 63) / 64;  // d = 96: 2, the last half zeros
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kKOff = 0;
@@ -440,7 +440,10 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   {
     LaunchProbe probe(kKindBwdPre, stream);
     const unsigned blocks = unsigned(p.sh.tq * kTile / kPreRows) * unsigned(p.sh.bh);
-    fa_bwd_pre<D, kF16><<<blocks, 256, 0, stream>>>(p);
+    // the preprocess reduces a row over a power-of-two number of lanes: a
+    // head dimension of 96 runs its d = 128 form (the last 4 lanes of a row
+    // add nothing)
+    fa_bwd_pre<(D == 96 ? 128 : D), kF16><<<blocks, 256, 0, stream>>>(p);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -470,7 +473,8 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
   const bool f16 = p.sh.f16 != 0;
   if (p.sh.d == 64) return f16 ? launch_bwd_d<64, true>(p, stream) : launch_bwd_d<64, false>(p, stream);
-  if (p.sh.d == 96 || p.sh.d == 128)
+  if (p.sh.d == 96) return f16 ? launch_bwd_d<96, true>(p, stream) : launch_bwd_d<96, false>(p, stream);
+  if (p.sh.d == 128)
     return f16 ? launch_bwd_d<128, true>(p, stream) : launch_bwd_d<128, false>(p, stream);
   if (p.sh.d == 256)
     return f16 ? launch_bwd_d<256, true>(p, stream) : launch_bwd_d<256, false>(p, stream);

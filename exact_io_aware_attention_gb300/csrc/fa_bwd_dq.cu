@@ -38,7 +38,7 @@ constexpr int kThreads = 384;
 
 template <int D>
 struct DqLayout {
-  static constexpr int kChunks = D / 64;
+  static constexpr int kChunks = (D + 63) / 64;  // d = 96: 2, the last half zeros
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kKSlots = 3, kVSlots = 2;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                                              status_code(kKernBwdDq, kRoleSoftmax, 4)));
     // tensor-memory loads are warp-wide; rows past the sequence end store nothing
     const bool live = qrow < sh.nq;
-    if (ok && D == 128 && count > 0) {
+    if (ok && D >= 96 && count > 0) {
       // each warpgroup's 64 columns leave through its chunk of the Q buffer,
       // which no MMA reads any more (count > 0: its Q load has landed; an
       // empty list stores its zeros directly below)
@@ -398,13 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                                i * kTile, h * 64, p.scale, count > 0, sh.d, sh.nq, h_idx, b_idx);
     } else if (ok) {
       tc_fence_after();
-      constexpr int kHalf = D / 2;
+      // the first warpgroup takes columns [0, kHalf), the second [kHalf, D)
+      constexpr int kHalf = D == 64 ? 32 : 64;
       uint16_t *dst_row =
           static_cast<uint16_t *>(p.dq) + p.sdq.row(b_idx, h_idx, qrow) + h * kHalf;
       const float sc = p.scale;
 #pragma unroll
       for (int q = 0; q < kHalf / 32; ++q) {
-        if (D == 128 && h * kHalf + q * 32 >= sh.d) break;  // head dimension 96
+        if (h * kHalf + q * 32 >= D) break;  // head dimension 96: 32 columns in the second half
         float v[32];
         if (count > 0) {
           ld_cols32(t + L::kColDQ + h * kHalf + 32 * q, v);
@@ -452,7 +453,8 @@ cudaError_t launch_dq_d(const BwdParams &p, cudaStream_t stream) {
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream) {
   const bool f16 = p.sh.f16 != 0;
   if (p.sh.d == 64) return f16 ? launch_dq_d<64, true>(p, stream) : launch_dq_d<64, false>(p, stream);
-  if (p.sh.d == 96 || p.sh.d == 128)
+  if (p.sh.d == 96) return f16 ? launch_dq_d<96, true>(p, stream) : launch_dq_d<96, false>(p, stream);
+  if (p.sh.d == 128)
     return f16 ? launch_dq_d<128, true>(p, stream) : launch_dq_d<128, false>(p, stream);
   return cudaErrorInvalidValue;
 }

@@ -53,10 +53,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the ma
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kChunks = D / 64;              // 128-byte column chunks per row
+  static constexpr int kChunks = (D + 63) / 64;       // 128-byte column chunks per row (d = 96: 2, the last half zeros)
   static constexpr int kChunkBytes = kTile * 128;     // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 5 : 10;  // K/V ring slots (K and V alternate)
+  static constexpr int kStages = (kChunks == 2) ? 5 : 10;  // K/V ring slots (K and V alternate)
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
   static constexpr int kListOff = kKVOff + kStages * kTileBytes;
@@ -71,7 +71,7 @@ struct FwdLayout {
   // O_t += P_t V. With d = 128 the 512 columns hold S_0, S_1, O_0, O_1 and P_t
   // takes the first half of S_t's columns once S_t has been read; with d = 64
   // it has columns of its own.
-  __host__ __device__ static constexpr uint32_t col_p(int t) { return D == 128 ? t * kTile : 384 + 64 * t; }
+  __host__ __device__ static constexpr uint32_t col_p(int t) { return D >= 96 ? t * kTile : 384 + 64 * t; }
 };
 
 struct Bars {
@@ -620,7 +620,8 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
 cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream) {
   const bool f16 = p.sh.f16 != 0;
   if (p.sh.d == 64) return f16 ? launch_fwd_d<64, true>(p, stream) : launch_fwd_d<64, false>(p, stream);
-  if (p.sh.d == 96 || p.sh.d == 128)
+  if (p.sh.d == 96) return f16 ? launch_fwd_d<96, true>(p, stream) : launch_fwd_d<96, false>(p, stream);
+  if (p.sh.d == 128)
     return f16 ? launch_fwd_d<128, true>(p, stream) : launch_fwd_d<128, false>(p, stream);
   if (p.sh.d == 256) {  // its own kernel (fa_fwd_d256.cu); the merge is shared
     cudaError_t e = launch_forward_d256(p, stream);

@@ -7,15 +7,16 @@
 
 namespace fa {
 
-// Row r of a 128-row tile: kCols fp32 columns (a multiple of 64) read from
+// Row r of a 128-row tile: kCols fp32 columns (a multiple of 32) read from
 // tensor memory at `tacc` (this warp's lane quadrant already in the address),
 // times `sc`, rounded to the 16-bit type (kF16: f16, else bf16) and written
 // to shared memory at `s_tile` as 64-column chunks of 128 rows x 128 bytes in
 // the 128-byte swizzle of the tensor maps; then lane 0 of the warp stores its
 // 32 rows through `tm` (a map with 64 x 32 boxes) at columns x0.. and rows
 // tile_row0 + ... of head (h_idx, b_idx). Columns at or past `d_cols` are
-// neither read nor stored (head dimension 96 runs as 128), and the map clips
-// rows at or past the tensor's row count; a warp whose first row is at or past
+// neither read nor stored, and the map clips rows at or past the tensor's row
+// count and columns past its width (a last chunk of 32 columns stores 64, of
+// which the map writes the first 32); a warp whose first row is at or past
 // `n_rows` stores nothing. With any == false the row is zero.
 //
 // Every thread of the warp must call it (tensor-memory loads are warp-wide),
@@ -27,7 +28,7 @@ __device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc
                                             uint32_t s_tile, int r, int tile_row0, int x0,
                                             float sc, bool any, int d_cols, int n_rows,
                                             int h_idx, int b_idx) {
-  static_assert(kCols % 64 == 0, "whole 64-column chunks");
+  static_assert(kCols % 32 == 0, "whole 32-column groups");
   constexpr uint32_t kChunkBytes = kTile * 128;
 #pragma unroll
   for (int q = 0; q < kCols / 32; ++q) {
@@ -55,7 +56,7 @@ __device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc
   fence_proxy_async_smem();
   __syncwarp();
   if ((r & 31) == 0 && tile_row0 + warp_row < n_rows) {
-    for (int c = 0; c < kCols / 64 && x0 + c * 64 < d_cols; ++c)
+    for (int c = 0; c < (kCols + 63) / 64 && x0 + c * 64 < d_cols; ++c)
       tma_store_4d(tm, s_tile + c * kChunkBytes + warp_row * 128, x0 + c * 64,
                    tile_row0 + warp_row, h_idx, b_idx);
     bulk_commit_group();
