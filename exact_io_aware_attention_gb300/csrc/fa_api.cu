@@ -223,7 +223,8 @@ fa_status input_dtype(const fa_tensor *Q, int *elem) {
   return FA_OK;
 }
 
-// Columns the kernels hold per row: a head dimension of 96 runs as 128.
+// Columns per row the split-forward workspace reserves: 128 for a head
+// dimension of 96 (the kernels use the first 96).
 int padded_d(int d) { return d == 96 ? 128 : d; }
 
 // Bytes of one part of the split-forward workspace (256-byte aligned parts).

@@ -110,9 +110,6 @@ __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
 }
 
-// kF16: f16 elements instead of bf16. D is 64 or 128; a head dimension of 96
-// runs as 128 (the tensor maps read zeros in columns 96..127) and only the
-// first sh.d columns of dK and dV are stored.
 // Stage s of the Q_i, dO_i ring, with LSE_i * log2(e) and D_i, onto q_full(s).
 template <int D>
 __device__ __forceinline__ void load_q_stage(const BwdParams &p, const Bars &bars, int s, int i,
@@ -132,6 +129,9 @@ __device__ __forceinline__ void load_q_stage(const BwdParams &p, const Bars &bar
   bulk_load_1d(sst + kTile * 4, p.delta + srow, kTile * 4, bars.q_full(s));
 }
 
+// kF16: f16 elements instead of bf16. D is 64, 96 or 128: at 96 the tiles keep two 64-column
+// chunks (the tensor maps read zeros in columns 96..127), the MMAs run 6 K-steps over the head
+// dimension and N = 96, and 96 columns of dK and dV are stored.
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant__ BwdParams p) {
   using L = DkdvLayout<D>;

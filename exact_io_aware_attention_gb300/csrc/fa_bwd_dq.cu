@@ -85,9 +85,9 @@ __device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
 }
 
-// kF16: f16 elements instead of bf16. D is 64 or 128; a head dimension of 96
-// runs as 128 (the tensor maps read zeros in columns 96..127) and only the
-// first sh.d columns of dQ are stored.
+// kF16: f16 elements instead of bf16. D is 64, 96 or 128: at 96 the tiles keep two 64-column
+// chunks (the tensor maps read zeros in columns 96..127), the MMAs run 6 K-steps over the head
+// dimension and N = 96, and 96 columns of dQ are stored.
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<D>;

@@ -94,12 +94,11 @@ __device__ __forceinline__ bool entry_act(uint32_t e, int t) { return (e >> (14 
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 
-// kSplit: the keys are split over p.n_split CTAs per Q-tile pair and the
-// epilogue writes this split's partial result (a separate instantiation, so
-// the plain forward carries none of it). kF16: f16 elements instead of bf16
-// (Q, K, V, P and a 16-bit O). D is 64 or 128; a head dimension of 96 runs
-// as 128, the tensor maps reading zeros in columns 96..127, and only the
-// first sh.d columns are stored.
+// kSplit: the keys are split over p.n_split CTAs per Q-tile pair and the epilogue writes this
+// split's partial result (a separate instantiation, so the plain forward carries none of it).
+// kF16: f16 elements instead of bf16 (Q, K, V, P and a 16-bit O). D is 64, 96 or 128: at 96 the
+// tiles keep two 64-column chunks (the tensor maps read zeros in columns 96..127), the MMAs run 6
+// K-steps over the head dimension and N = 96 (the PV MMA), and 96 columns of O are stored.
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
@@ -487,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         } else {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
-            if (D == 128 && q * 32 >= sh.d) break;  // head dimension 96: columns 96..127 unused
             uint32_t o[32];
             if (any) {
               tmem_ld32(tO + q * 32, o);

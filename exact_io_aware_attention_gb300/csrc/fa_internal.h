@@ -29,7 +29,7 @@ struct RowStrides {
 struct Shape {
   int bh, heads;                      // B*H and H (bh = b * heads + h)
   int nq, nk, tq, tk;
-  int d, causal, causal_off;          // d: the head dimension (the kernels run 96 as 128)
+  int d, causal, causal_off;          // d: the head dimension (64, 96, 128 or 256)
   int f16;                            // 16-bit element type: 1 = f16, 0 = bf16
   const uint8_t *mask;                // [tq][tk] or null
 

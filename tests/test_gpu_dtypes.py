@@ -2,8 +2,9 @@
 
 fp16: Q, K, V, dO are N(0, 1) rounded to fp16; the tensor cores multiply in
 fp16 (P and dS rounded to fp16) and accumulate in fp32, and O, dQ, dK, dV are
-fp16. Head dimension 96 runs on the 128-column kernels with zero columns
-96..127 read from the tensor maps; only 96 columns are stored. The oracle
+fp16. Head dimension 96 has its own kernel instantiations: tiles of two
+64-column chunks with zero columns 96..127 read from the tensor maps, 6
+K-steps and N = 96 in the MMAs, 96 columns stored. The oracle
 sees the same inputs, widened exactly to fp64. Tolerances are those of the
 bf16 tests (fp16 has three more mantissa bits, so the errors are smaller)."""
 import numpy as np
