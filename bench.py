@@ -174,9 +174,9 @@ def summarize_clocks(rows):
 # Source files each measured kernel is compiled from (its own file and the
 # shared headers): a committed ncu capture is valid while they are unchanged.
 KERNEL_SOURCES = {
-    "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
-    "fa_bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
-    "fa_bwd_dq": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.h"),
+    "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
+    "fa_bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
+    "fa_bwd_dq": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
 }
 
 
