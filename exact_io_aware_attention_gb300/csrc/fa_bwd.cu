@@ -102,14 +102,6 @@ __device__ __forceinline__ int next_q(const Shape &sh, int i, int j) {
 // (queries 16kk..16kk+15): queries 64h.. are packed at column 64h.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-  tmem_wait_ld();
-#pragma unroll
-  for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-}
-
 // Stage s of the Q_i, dO_i ring, with LSE_i * log2(e) and D_i, onto q_full(s).
 template <int D>
 __device__ __forceinline__ void load_q_stage(const BwdParams &p, const Bars &bars, int s, int i,
@@ -314,22 +306,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       tc_fence_after();
       const float *lse2 = stat + s * 2 * kTile + 64 * h;
       const float *delta = lse2 + kTile;
-      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e); on a tile that
-      // the causal boundary crosses, key kr sees query q only if q >= lo
-      const int lo = (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off)
-                         ? kTile * (j - i) + kr - sh.causal_off
-                         : 0;
+      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e): both loads in
+      // flight before the one wait
       float pr[64];
+      {
+        uint32_t sr[2][32];
+        tmem_ld32(t + L::kColS + 64 * h, sr[0]);
+        tmem_ld32(t + L::kColS + 64 * h + 32, sr[1]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float sv[32];
-        ld_cols32(t + L::kColS + 64 * h + 32 * q, sv);
+        for (int x = 0; x < 64; ++x)
+          pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x >> 5][x & 31]), c, -lse2[x]));
+      }
+      // only on a tile that the causal boundary crosses (one per K/V tile):
+      // key kr sees query 64h + x only if x >= lo
+      if (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off) {
+        const int lo = kTile * (j - i) + kr - sh.causal_off - 64 * h;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int col = 64 * h + 32 * q + x;
-          float v = ex2_approx(fmaf(sv[x], c, -lse2[32 * q + x]));
-          pr[32 * q + x] = (col < lo) ? 0.f : v;
-        }
+        for (int x = 0; x < 64; ++x)
+          if (x < lo) pr[x] = 0.f;
       }
       // P^T into tensor memory over this warpgroup's first 32 S^T columns
       {
@@ -347,14 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[32];
+      {
+        uint32_t dr[2][32];
+        tmem_ld32(t + L::kColDP + 64 * h, dr[0]);
+        tmem_ld32(t + L::kColDP + 64 * h + 32, dr[1]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float dp[32];
-        ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
-#pragma unroll
-        for (int x = 0; x < 32; x += 2)
-          dsp[16 * q + x / 2] = pack2<kF16>(pr[32 * q + x] * (dp[x] - delta[32 * q + x]),
-                                            pr[32 * q + x + 1] * (dp[x + 1] - delta[32 * q + x + 1]));
+        for (int x = 0; x < 64; x += 2)
+          dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x >> 5][x & 31]) - delta[x]),
+                                   pr[x + 1] * (__uint_as_float(dr[x >> 5][(x + 1) & 31]) - delta[x + 1]));
       }
       tmem_st32(t + L::kColDP + 64 * h, dsp);
       tmem_wait_st();

@@ -337,20 +337,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       tc_fence_after();
       float pr[64];
       {
-        float s0[32], s1[32];
-        ld_cols32(t + L::kColS + 64 * h, s0);
-        ld_cols32(t + L::kColS + 64 * h + 32, s1);
+        // both loads in flight before the one wait
+        uint32_t sr[2][32];
+        tmem_ld32(t + L::kColS + 64 * h, sr[0]);
+        tmem_ld32(t + L::kColS + 64 * h + 32, sr[1]);
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bars.s_free());
-        const uint32_t e = list[n];
-        // keys x >= lim of this tile are hidden from this row
-        const int lim = (e >> 15) ? sh.key_limit(i, r, int(e & 0x7FFF)) - 64 * h : 64;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          pr[x] = ex2_approx(fmaf(s0[x], c, -lse2));
-          pr[32 + x] = ex2_approx(fmaf(s1[x], c, -lse2));
-          if (x >= lim) pr[x] = 0.f;
-          if (32 + x >= lim) pr[32 + x] = 0.f;
+        for (int x = 0; x < 64; ++x) pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x >> 5][x & 31]), c, -lse2));
+      }
+      {
+        const uint32_t e = list[n];
+        if (e >> 15) {  // a partial tile: keys x >= lim of this half are hidden from this row
+          const int lim = sh.key_limit(i, r, int(e & 0x7FFF)) - 64 * h;
+#pragma unroll
+          for (int x = 0; x < 64; ++x)
+            if (x >= lim) pr[x] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
@@ -358,18 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[32];  // dS as packed 16-bit pairs: keys (2x, 2x+1) of this half
+      {
+        uint32_t dr[2][32];
+        tmem_ld32(t + L::kColDP + 64 * h, dr[0]);
+        tmem_ld32(t + L::kColDP + 64 * h + 32, dr[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bars.dp_free());
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float dp[32];
-        ld_cols32(t + L::kColDP + 64 * h + 32 * q, dp);
-        if (q == 1) {
-          tc_fence_before();
-          mbar_arrive(bars.dp_free());
-        }
-#pragma unroll
-        for (int x = 0; x < 32; x += 2)
-          dsp[16 * q + x / 2] = pack2<kF16>(pr[32 * q + x] * (dp[x] - dd),
-                                            pr[32 * q + x + 1] * (dp[x + 1] - dd));
+        for (int x = 0; x < 64; x += 2)
+          dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x >> 5][x & 31]) - dd),
+                                   pr[x + 1] * (__uint_as_float(dr[x >> 5][(x + 1) & 31]) - dd));
       }
       const int b = n & 1;
       if (n >= 2) {
