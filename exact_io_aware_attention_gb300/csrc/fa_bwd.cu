@@ -40,11 +40,12 @@
 // (d columns each). P^T and dS^T (16-bit pairs) are the tensor-memory A
 // operands of dV += P^T dO and dK += dS^T Q: the warpgroup for queries
 // 64h..64h+63 writes them over the first 32 of its own 64 S^T (dP^T)
-// columns once it has read them. Shared memory: K_j, V_j, Q_i[2], dO_i[2],
-// LSE and D of the current step. MMA order per step n: dV(n), S^T(n+1),
-// dK(n), dP^T(n+1); MMAs issued by one thread execute in issue order, so
-// S^T(n+1) and dP^T(n+1) overwrite P^T(n) and dS^T(n) only after dV(n) and
-// dK(n) have read them.
+// columns once it has read them. P^T goes out in two halves of 32 queries,
+// each on its own barrier, and dV(n) is issued in the same two halves.
+// Shared memory: K_j, V_j, Q_i[2], dO_i[2], LSE and D of the current step.
+// MMA order per step n: dV(n), S^T(n+1), dK(n), dP^T(n+1); MMAs issued by
+// one thread execute in issue order, so S^T(n+1) and dP^T(n+1) overwrite
+// P^T(n) and dS^T(n) only after dV(n) and dK(n) have read them.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -81,7 +82,8 @@ struct Bars {
   __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
   __device__ uint32_t q_empty(int s) const { return base + 8 * (3 + s); }
   __device__ uint32_t s_full() const { return base + 8 * 5; }
-  __device__ uint32_t p_full() const { return base + 8 * 6; }
+  // P^T of queries 64h + 32u .. 64h + 32u + 31 of both warpgroups h (u = 0, 1)
+  __device__ uint32_t p_full(int u) const { return base + 8 * (u ? 8 : 6); }
   __device__ uint32_t dp_full() const { return base + 8 * 7; }
   __device__ uint32_t ds_full() const { return base + 8 * 9; }
   __device__ uint32_t acc_done() const { return base + 8 * 11; }
@@ -167,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       mbar_init(bars.q_empty(s), 1);
     }
     mbar_init(bars.s_full(), 1);
-    mbar_init(bars.p_full(), 256);
+    mbar_init(bars.p_full(0), 256);
+    mbar_init(bars.p_full(1), 256);
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.ds_full(), 256);
     mbar_init(bars.acc_done(), 1);
@@ -236,13 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         }
       };
       // acc += X Y with X = P^T (or dS^T) packed in tensor memory at a_col and
-      // Y with queries as K (MN-major, 16 query rows per step)
-      auto issue_acc = [&](uint32_t a_col, uint32_t y_base, uint32_t col, bool first) {
+      // Y with queries as K (MN-major, 16 query rows per step), over the
+      // queries 64h + 32u .. 64h + 32u + 31 of both warpgroups h
+      auto issue_acc = [&](uint32_t a_col, uint32_t y_base, uint32_t col, bool first, int u) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
+        for (int e = 0; e < 4; ++e) {
+          const int kk = (e >> 1) * 4 + 2 * u + (e & 1);
           mma_f16kind_ts(tmem + col, tmem + a_col + packed_col(kk),
                       sdesc_sw128(y_base + kk * 2048, L::kChunkBytes, 1024), kIdAcc,
-                      (!first || kk > 0) ? 1u : 0u);
+                      (!first || u > 0 || e > 0) ? 1u : 0u);
+        }
       };
       if (ok && any) {
         ok = mbar_wait(bars.q_full(0), 0, st, status_code(kKernBwd, kRoleMma, 2));
@@ -258,10 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       for (int i = first; i < T && ok; ++n) {
         const int s = n & 1, s1 = s ^ 1;
         const int inext = next_q(sh, i + 1, j);
-        ok = mbar_wait(bars.p_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
+        // dV(n) in two halves: the first runs while the softmax warps finish
+        // the second half of P^T(n)
+        ok = mbar_wait(bars.p_full(0), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0);
+        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0, 0);
+        ok = mbar_wait(bars.p_full(1), n & 1, st, status_code(kKernBwd, kRoleMma, 6));
+        if (!ok) break;
+        tc_fence_after();
+        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0, 1);
         // dV is final after the last step's dV MMA: its epilogue need not
         // wait for the last dK
         if (inext >= T) mma_commit(bars.dv_done());
@@ -275,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 5));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0);
+        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0, 0);
+        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0, 1);
         mma_commit(bars.q_empty(s));
         if (inext < T) {
           issue_sq(sV, sdO + s1 * L::kTileBytes, L::kColDP);
@@ -306,36 +319,39 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       tc_fence_after();
       const float *lse2 = stat + s * 2 * kTile + 64 * h;
       const float *delta = lse2 + kTile;
-      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e): both loads in
-      // flight before the one wait
+      // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e), in two halves of
+      // 32 queries, each written to tensor memory (over this warpgroup's
+      // first 32 S^T columns, already read) and announced on its own barrier
+      // so that dV's MMAs over the first half can start early
       float pr[64];
       {
         uint32_t sr[2][32];
         tmem_ld32(t + L::kColS + 64 * h, sr[0]);
         tmem_ld32(t + L::kColS + 64 * h + 32, sr[1]);
         tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 64; ++x)
-          pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x >> 5][x & 31]), c, -lse2[x]));
-      }
-      // only on a tile that the causal boundary crosses (one per K/V tile):
-      // key kr sees query 64h + x only if x >= lo
-      if (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off) {
+        // only on a tile that the causal boundary crosses (one per K/V
+        // tile): key kr sees query 64h + x only if x >= lo
+        const bool cross = sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off;
         const int lo = kTile * (j - i) + kr - sh.causal_off - 64 * h;
 #pragma unroll
-        for (int x = 0; x < 64; ++x)
-          if (x < lo) pr[x] = 0.f;
-      }
-      // P^T into tensor memory over this warpgroup's first 32 S^T columns
-      {
-        uint32_t pk[32];
+        for (int u = 0; u < 2; ++u) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) pk[x] = pack2<kF16>(pr[2 * x], pr[2 * x + 1]);
-        tmem_st32(t + L::kColS + 64 * h, pk);
-        tmem_wait_st();
+          for (int x = 32 * u; x < 32 * u + 32; ++x)
+            pr[x] = ex2_approx(fmaf(__uint_as_float(sr[u][x & 31]), c, -lse2[x]));
+          if (cross) {
+#pragma unroll
+            for (int x = 32 * u; x < 32 * u + 32; ++x)
+              if (x < lo) pr[x] = 0.f;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[x] = pack2<kF16>(pr[32 * u + 2 * x], pr[32 * u + 2 * x + 1]);
+          tmem_st16(t + L::kColS + 64 * h + 16 * u, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bars.p_full(u));
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bars.p_full());
       // dS^T_kq = P^T_kq (dP^T_kq - D_q) into tensor memory over dP^T
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 4)));

@@ -57,14 +57,6 @@ constexpr int kHalfBytes = 2 * kChunkBytes;  // 128 rows x 128 columns: one ring
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
 
-__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-  tmem_wait_ld();
-#pragma unroll
-  for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-}
-
 // Tensor-memory column of the packed A operand (P^T, dS^T or dS) for MMA
 // step kk (columns 16kk..16kk+15 of the 128 x 128 tile): the warpgroup that
 // owns columns 64h..64h+63 packs them at column 64h.
@@ -384,25 +376,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
       if (!ok) break;
       tc_fence_after();
       const float *lse2 = stat + b * kTile + 64 * h;
-      // on a tile that the causal boundary crosses, key kr sees query x only if x >= lo
-      const int lo = (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off)
-                         ? kTile * (j - i) + kr - sh.causal_off
-                         : 0;
+      float pr[64];
+      {
+        // both loads in flight before the one wait
+        uint32_t sr[2][32];
+        tmem_ld32(t + b * kTile + 64 * h, sr[0]);
+        tmem_ld32(t + b * kTile + 64 * h + 32, sr[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x >> 5][x & 31]), c, -lse2[x]));
+      }
+      // only on a tile that the causal boundary crosses: key kr sees query
+      // 64h + x only if x >= lo
+      if (sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off) {
+        const int lo = kTile * (j - i) + kr - sh.causal_off - 64 * h;
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (x < lo) pr[x] = 0.f;
+      }
       uint32_t pk[32];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float sv[32];
-        ld_cols32(t + b * kTile + 64 * h + 32 * q, sv);
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int col = 64 * h + 32 * q + x;
-          float p0 = ex2_approx(fmaf(sv[x], c, -lse2[32 * q + x]));
-          float p1 = ex2_approx(fmaf(sv[x + 1], c, -lse2[32 * q + x + 1]));
-          if (col < lo) p0 = 0.f;
-          if (col + 1 < lo) p1 = 0.f;
-          pk[16 * q + x / 2] = pack2<kF16>(p0, p1);
-        }
-      }
+      for (int x = 0; x < 32; ++x) pk[x] = pack2<kF16>(pr[2 * x], pr[2 * x + 1]);
       // P^T over the first 32 of this warpgroup's S^T columns (already read)
       tmem_st32(t + b * kTile + 64 * h, pk);
       tmem_wait_st();
@@ -731,45 +726,56 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
                                                        status_code(kKern, kRoleSoftmax, 2)));
       if (!ok) break;
       tc_fence_after();
-      float s0[32], s1[32];
-      ld_cols32(t + L::kColX + 64 * h, s0);
-      ld_cols32(t + L::kColX + 64 * h + 32, s1);
-      tc_fence_before();
-      mbar_arrive(bars.x_free());
-      // visible columns of this tile: lo <= col < lim
-      int lo = 0, lim = kTile;
       const float *lse2c = stat + (n & 1) * 2 * kTile + 64 * h;  // dK: per-column statistics
       const float *dc = lse2c + kTile;
-      if constexpr (kKeys) {
-        // key row r of tile rt sees query col of tile x iff col >= lo
-        if (sh.causal && kTile * rt + kTile - 1 > kTile * x + sh.causal_off)
-          lo = kTile * (rt - x) + r - sh.causal_off;
-      } else {
-        if (sh.partial(rt, x)) lim = sh.key_limit(rt, r, x);
-      }
       float pr[64];
+      {
+        // both loads in flight before the one wait
+        uint32_t sr[2][32];
+        tmem_ld32(t + L::kColX + 64 * h, sr[0]);
+        tmem_ld32(t + L::kColX + 64 * h + 32, sr[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bars.x_free());
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const int col = 64 * h + k;
-        const float sv = k < 32 ? s0[k] : s1[k - 32];
-        const float v = ex2_approx(fmaf(sv, c, kKeys ? -lse2c[k] : -lse2_row));
-        pr[k] = (col < lo || col >= lim) ? 0.f : v;
+        for (int k = 0; k < 64; ++k)
+          pr[k] = ex2_approx(fmaf(__uint_as_float(sr[k >> 5][k & 31]), c,
+                                  kKeys ? -lse2c[k] : -lse2_row));
+      }
+      // the mask, only on the tiles it touches
+      if constexpr (kKeys) {
+        // key row r of tile rt sees query 64h + k of tile x iff k >= lo
+        if (sh.causal && kTile * rt + kTile - 1 > kTile * x + sh.causal_off) {
+          const int lo = kTile * (rt - x) + r - sh.causal_off - 64 * h;
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k < lo) pr[k] = 0.f;
+        }
+      } else {
+        // keys 64h + k >= key_limit of tile x are hidden from query row r
+        if (sh.partial(rt, x)) {
+          const int lim = sh.key_limit(rt, r, x) - 64 * h;
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k >= lim) pr[k] = 0.f;
+        }
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bars.y_full(), n & 1, st,
                                              status_code(kKern, kRoleSoftmax, 3)));
       if (!ok) break;
       tc_fence_after();
       uint32_t ep[32];
+      {
+        uint32_t dr[2][32];
+        tmem_ld32(t + L::kColY + 64 * h, dr[0]);
+        tmem_ld32(t + L::kColY + 64 * h + 32, dr[1]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float dp[32];
-        ld_cols32(t + L::kColY + 64 * h + 32 * q, dp);
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float d0 = kKeys ? dc[32 * q + k] : d_row;
-          const float d1 = kKeys ? dc[32 * q + k + 1] : d_row;
-          ep[16 * q + k / 2] = pack2<kF16>(pr[32 * q + k] * (dp[k] - d0),
-                                           pr[32 * q + k + 1] * (dp[k + 1] - d1));
+        for (int k = 0; k < 64; k += 2) {
+          const float d0 = kKeys ? dc[k] : d_row;
+          const float d1 = kKeys ? dc[k + 1] : d_row;
+          ep[k / 2] = pack2<kF16>(pr[k] * (__uint_as_float(dr[k >> 5][k & 31]) - d0),
+                                  pr[k + 1] * (__uint_as_float(dr[k >> 5][(k + 1) & 31]) - d1));
         }
       }
       // E over the first 32 of this warpgroup's Y columns (already read)
