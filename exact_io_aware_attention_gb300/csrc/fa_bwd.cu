@@ -31,7 +31,8 @@
 // key row only feeds its own dK/dV row, which is not stored.
 //
 // fa_bwd_dkdv, 12 warps:
-//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per step (2 stages)
+//   warp 0      TMA producer: K_j, V_j once; per step Q_i with LSE_i (3 slots) and
+//               dO_i with D_i (2 slots)
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
 //   warps 4-7   thread = key row: P^T and dS^T for queries 0..63; then dV out
 //               (once the last dV MMA has completed: dv_done)
@@ -42,7 +43,9 @@
 // 64h..64h+63 writes them over the first 32 of its own 64 S^T (dP^T)
 // columns once it has read them. P^T goes out in two halves of 32 queries,
 // each on its own barrier, and dV(n) is issued in the same two halves.
-// Shared memory: K_j, V_j, Q_i[2], dO_i[2], LSE and D of the current step.
+// Shared memory: K_j, V_j, Q_i[3] with LSE_i, dO_i[2] with D_i. A Q slot is
+// free once dK has read it; a dO slot once dV has read dO_i and the softmax
+// warps have read D_i, so Q_{n+2} loads while step n is still running.
 // MMA order per step n: dV(n), S^T(n+1), dK(n), dP^T(n+1); MMAs issued by
 // one thread execute in issue order, so S^T(n+1) and dP^T(n+1) overwrite
 // P^T(n) and dS^T(n) only after dV(n) and dK(n) have read them.
@@ -62,14 +65,15 @@ struct DkdvLayout {
   static constexpr int kChunks = (D + 63) / 64;  // d = 96: 2, the last half zeros
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kQSlots = 3, kdOSlots = 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kQOff = kVOff + kTileBytes;       // 2 stages
-  static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // 2 stages
-  static constexpr int kStatOff = kdOOff + 2 * kTileBytes; // [2 stages][lse2 128 | delta 128] fp32
-  static constexpr int kStatBytes = 2 * kTile * 4;
-  static constexpr int kBarOff = kStatOff + 2 * kStatBytes;
-  static constexpr int kNumBars = 15;
+  static constexpr int kQOff = kVOff + kTileBytes;
+  static constexpr int kdOOff = kQOff + kQSlots * kTileBytes;
+  static constexpr int kLseOff = kdOOff + kdOSlots * kTileBytes;  // [kQSlots][128] LSE * log2(e)
+  static constexpr int kDeltaOff = kLseOff + kQSlots * kTile * 4;  // [kdOSlots][128] D
+  static constexpr int kBarOff = kDeltaOff + kdOSlots * kTile * 4;
+  static constexpr int kNumBars = 19;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -79,16 +83,19 @@ struct DkdvLayout {
 struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
+  // Q slot s (Q_i with LSE_i) and dO slot s (dO_i with D_i)
   __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t q_empty(int s) const { return base + 8 * (3 + s); }
-  __device__ uint32_t s_full() const { return base + 8 * 5; }
+  __device__ uint32_t q_empty(int s) const { return base + 8 * (4 + s); }
+  __device__ uint32_t do_full(int s) const { return base + 8 * (7 + s); }
+  __device__ uint32_t do_empty(int s) const { return base + 8 * (9 + s); }
+  __device__ uint32_t s_full() const { return base + 8 * 11; }
   // P^T of queries 64h + 32u .. 64h + 32u + 31 of both warpgroups h (u = 0, 1)
-  __device__ uint32_t p_full(int u) const { return base + 8 * (u ? 8 : 6); }
-  __device__ uint32_t dp_full() const { return base + 8 * 7; }
-  __device__ uint32_t ds_full() const { return base + 8 * 9; }
-  __device__ uint32_t acc_done() const { return base + 8 * 11; }
-  __device__ uint32_t teardown() const { return base + 8 * 12; }
-  __device__ uint32_t dv_done() const { return base + 8 * 13; }
+  __device__ uint32_t p_full(int u) const { return base + 8 * (12 + u); }
+  __device__ uint32_t dp_full() const { return base + 8 * 14; }
+  __device__ uint32_t ds_full() const { return base + 8 * 15; }
+  __device__ uint32_t acc_done() const { return base + 8 * 16; }
+  __device__ uint32_t teardown() const { return base + 8 * 17; }
+  __device__ uint32_t dv_done() const { return base + 8 * 18; }
 };
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
@@ -104,23 +111,30 @@ __device__ __forceinline__ int next_q(const Shape &sh, int i, int j) {
 // (queries 16kk..16kk+15): queries 64h.. are packed at column 64h.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// Stage s of the Q_i, dO_i ring, with LSE_i * log2(e) and D_i, onto q_full(s).
+// Q tile i with LSE_i * log2(e) into Q slot s, onto q_full(s).
 template <int D>
-__device__ __forceinline__ void load_q_stage(const BwdParams &p, const Bars &bars, int s, int i,
-                                             uint32_t s_base, uint32_t sQ, uint32_t sdO,
-                                             size_t stat_head, int h_idx, int b_idx) {
+__device__ __forceinline__ void load_q(const BwdParams &p, const Bars &bars, int s, int i,
+                                       uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
   using L = DkdvLayout<D>;
-  mbar_arrive_expect_tx(bars.q_full(s), 2 * L::kTileBytes + L::kStatBytes);
-  for (int c = 0; c < L::kChunks; ++c) {
-    tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64, i * kTile, h_idx,
-                b_idx, bars.q_full(s));
-    tma_load_4d(sdO + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64, i * kTile, h_idx,
-                b_idx, bars.q_full(s));
-  }
-  const uint32_t sst = s_base + L::kStatOff + s * L::kStatBytes;
-  const size_t srow = stat_head + (size_t)i * kTile;
-  bulk_load_1d(sst, p.lse2 + srow, kTile * 4, bars.q_full(s));
-  bulk_load_1d(sst + kTile * 4, p.delta + srow, kTile * 4, bars.q_full(s));
+  mbar_arrive_expect_tx(bars.q_full(s), L::kTileBytes + kTile * 4);
+  for (int c = 0; c < L::kChunks; ++c)
+    tma_load_4d(s_base + L::kQOff + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, c * 64,
+                i * kTile, h_idx, b_idx, bars.q_full(s));
+  bulk_load_1d(s_base + L::kLseOff + s * kTile * 4, p.lse2 + stat_head + (size_t)i * kTile,
+               kTile * 4, bars.q_full(s));
+}
+
+// dO tile i with D_i into dO slot s, onto do_full(s).
+template <int D>
+__device__ __forceinline__ void load_do(const BwdParams &p, const Bars &bars, int s, int i,
+                                        uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
+  using L = DkdvLayout<D>;
+  mbar_arrive_expect_tx(bars.do_full(s), L::kTileBytes + kTile * 4);
+  for (int c = 0; c < L::kChunks; ++c)
+    tma_load_4d(s_base + L::kdOOff + s * L::kTileBytes + c * L::kChunkBytes, &p.tm_do, c * 64,
+                i * kTile, h_idx, b_idx, bars.do_full(s));
+  bulk_load_1d(s_base + L::kDeltaOff + s * kTile * 4, p.delta + stat_head + (size_t)i * kTile,
+               kTile * 4, bars.do_full(s));
 }
 
 // kF16: f16 elements instead of bf16. D is 64, 96 or 128: at 96 the tiles keep two 64-column
@@ -140,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   }
   const uint32_t sK = s_base + L::kKOff, sV = s_base + L::kVOff;
   const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff;
-  const float *stat = reinterpret_cast<const float *>(smem + L::kStatOff);
+  const float *lse_s = reinterpret_cast<const float *>(smem + L::kLseOff);
+  const float *delta_s = reinterpret_cast<const float *>(smem + L::kDeltaOff);
   Bars bars{s_base + L::kBarOff};
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
 
@@ -164,9 +179,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 
   if (warp == 0 && (threadIdx.x & 31) == 0) {
     mbar_init(bars.kv_full(), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::kQSlots; ++s) {
       mbar_init(bars.q_full(s), 1);
       mbar_init(bars.q_empty(s), 1);
+    }
+    // a dO slot is free once dV has read dO_i (one commit) and the softmax
+    // warps have read D_i (256 threads)
+    for (int s = 0; s < L::kdOSlots; ++s) {
+      mbar_init(bars.do_full(s), 1);
+      mbar_init(bars.do_empty(s), 257);
     }
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.p_full(0), 256);
@@ -192,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         tma_load_4d(sV + c * L::kChunkBytes, &p.tm_v, c * 64, j * kTile, h_idx, b_idx,
                     bars.kv_full());
       }
-      load_q_stage<D>(p, bars, 0, first, s_base, sQ, sdO, stat_head, h_idx, b_idx);
+      load_q<D>(p, bars, 0, first, s_base, stat_head, h_idx, b_idx);
+      load_do<D>(p, bars, 0, first, s_base, stat_head, h_idx, b_idx);
     }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
@@ -206,20 +228,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
     if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
-      int n = 1;  // K, V and stage 0 (the first Q tile) were loaded during set-up
+      int nq = 1, ndo = 1;  // tiles issued: the first Q tile's Q and dO came with the set-up
       bool ok = true;
-      for (int i = next_q(sh, first + 1, j); i < T && ok; i = next_q(sh, i + 1, j), ++n) {
-        const int s = n & 1;
-        const uint32_t u = n >> 1;
-        ok = mbar_wait(bars.q_empty(s), (u & 1u) ^ 1u, st, status_code(kKernBwd, kRoleLoad, 1));
+      for (int i = next_q(sh, first + 1, j); i < T && ok; i = next_q(sh, i + 1, j)) {
+        const int qs = nq % L::kQSlots;
+        ok = mbar_wait(bars.q_empty(qs), ((nq / L::kQSlots) & 1u) ^ 1u, st,
+                       status_code(kKernBwd, kRoleLoad, 1));
         if (!ok) break;
-        load_q_stage<D>(p, bars, s, i, s_base, sQ, sdO, stat_head, h_idx, b_idx);
+        load_q<D>(p, bars, qs, i, s_base, stat_head, h_idx, b_idx);
+        ++nq;
+        const int ds = ndo % L::kdOSlots;
+        ok = mbar_wait(bars.do_empty(ds), ((ndo / L::kdOSlots) & 1u) ^ 1u, st,
+                       status_code(kKernBwd, kRoleLoad, 4));
+        if (!ok) break;
+        load_do<D>(p, bars, ds, i, s_base, stat_head, h_idx, b_idx);
+        ++ndo;
       }
       // teardown: every copy issued has landed
       mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleLoad, 2));
-      for (int s = 0; s < 2 && s < n; ++s) {
-        const int last = s + ((n - 1 - s) / 2) * 2;
-        mbar_wait(bars.q_full(s), (last >> 1) & 1u, st, status_code(kKernBwd, kRoleLoad, 3));
+      for (int s = 0; s < L::kQSlots && s < nq; ++s) {
+        const int last = s + ((nq - 1 - s) / L::kQSlots) * L::kQSlots;
+        mbar_wait(bars.q_full(s), (last / L::kQSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 3));
+      }
+      for (int s = 0; s < L::kdOSlots && s < ndo; ++s) {
+        const int last = s + ((ndo - 1 - s) / L::kdOSlots) * L::kdOSlots;
+        mbar_wait(bars.do_full(s), (last / L::kdOSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 5));
       }
     }
     __syncwarp();
@@ -256,45 +289,57 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
           tc_fence_after();
           issue_sq(sK, sQ, L::kColS);
           mma_commit(bars.s_full());
+          ok = mbar_wait(bars.do_full(0), 0, st, status_code(kKernBwd, kRoleMma, 7));
+        }
+        if (ok) {
+          tc_fence_after();
           issue_sq(sV, sdO, L::kColDP);
           mma_commit(bars.dp_full());
         }
       }
-      int n = 0;
+      int n = 0, qs = 0, qph = 0;  // Q slot of step n and the parity of its phase
       for (int i = first; i < T && ok; ++n) {
-        const int s = n & 1, s1 = s ^ 1;
+        const int ds = n & 1, ds1 = ds ^ 1;  // dO slots of steps n and n + 1
+        const int qs1 = qs + 1 == L::kQSlots ? 0 : qs + 1;
+        const int qph1 = qs + 1 == L::kQSlots ? qph ^ 1 : qph;
         const int inext = next_q(sh, i + 1, j);
         // dV(n) in two halves: the first runs while the softmax warps finish
         // the second half of P^T(n)
         ok = mbar_wait(bars.p_full(0), n & 1, st, status_code(kKernBwd, kRoleMma, 3));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0, 0);
+        issue_acc(L::kColS, sdO + ds * L::kTileBytes, L::kColDV, n == 0, 0);
         ok = mbar_wait(bars.p_full(1), n & 1, st, status_code(kKernBwd, kRoleMma, 6));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(L::kColS, sdO + s * L::kTileBytes, L::kColDV, n == 0, 1);
+        issue_acc(L::kColS, sdO + ds * L::kTileBytes, L::kColDV, n == 0, 1);
+        mma_commit(bars.do_empty(ds));  // dV(n) has read dO_n
         // dV is final after the last step's dV MMA: its epilogue need not
         // wait for the last dK
         if (inext >= T) mma_commit(bars.dv_done());
         if (inext < T) {
-          ok = mbar_wait(bars.q_full(s1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 4));
+          ok = mbar_wait(bars.q_full(qs1), qph1, st, status_code(kKernBwd, kRoleMma, 4));
           if (!ok) break;
           tc_fence_after();
-          issue_sq(sK, sQ + s1 * L::kTileBytes, L::kColS);
+          issue_sq(sK, sQ + qs1 * L::kTileBytes, L::kColS);
           mma_commit(bars.s_full());
         }
         ok = mbar_wait(bars.ds_full(), n & 1, st, status_code(kKernBwd, kRoleMma, 5));
         if (!ok) break;
         tc_fence_after();
-        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0, 0);
-        issue_acc(L::kColDP, sQ + s * L::kTileBytes, L::kColDK, n == 0, 1);
-        mma_commit(bars.q_empty(s));
+        issue_acc(L::kColDP, sQ + qs * L::kTileBytes, L::kColDK, n == 0, 0);
+        issue_acc(L::kColDP, sQ + qs * L::kTileBytes, L::kColDK, n == 0, 1);
+        mma_commit(bars.q_empty(qs));
         if (inext < T) {
-          issue_sq(sV, sdO + s1 * L::kTileBytes, L::kColDP);
+          ok = mbar_wait(bars.do_full(ds1), ((n + 1) >> 1) & 1, st, status_code(kKernBwd, kRoleMma, 7));
+          if (!ok) break;
+          tc_fence_after();
+          issue_sq(sV, sdO + ds1 * L::kTileBytes, L::kColDP);
           mma_commit(bars.dp_full());
         }
         i = inext;
+        qs = qs1;
+        qph = qph1;
       }
       if (ok) mma_commit(bars.acc_done());
       mma_commit(bars.teardown());
@@ -308,17 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
     const uint32_t t = tmem + (uint32_t((warp & 3) * 32) << 16);
     const float c = p.scale_log2;
     bool ok = true;
-    int n = 0;
+    int n = 0, qs = 0, qph = 0;  // Q slot of step n and the parity of its phase
     for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
-      const int s = n & 1;
+      const int ds = n & 1;  // dO slot
       ok = __all_sync(0xffffffffu, mbar_wait(bars.s_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 1)));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full(s), (n >> 1) & 1, st,
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full(qs), qph, st,
                                                      status_code(kKernBwd, kRoleSoftmax, 2)));
       if (!ok) break;
       tc_fence_after();
-      const float *lse2 = stat + s * 2 * kTile + 64 * h;
-      const float *delta = lse2 + kTile;
+      const float *lse2 = lse_s + qs * kTile + 64 * h;
+      const float *delta = delta_s + ds * kTile + 64 * h;
+      qph = qs + 1 == L::kQSlots ? qph ^ 1 : qph;
+      qs = qs + 1 == L::kQSlots ? 0 : qs + 1;
       // P^T_kq = exp2(s_kq * scale * log2e - LSE_q * log2e), in two halves of
       // 32 queries, each written to tensor memory (over this warpgroup's
       // first 32 S^T columns, already read) and announced on its own barrier
@@ -355,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       // dS^T_kq = P^T_kq (dP^T_kq - D_q) into tensor memory over dP^T
       ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), n & 1, st,
                                              status_code(kKernBwd, kRoleSoftmax, 4)));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bars.do_full(ds), (n >> 1) & 1, st,
+                                                     status_code(kKernBwd, kRoleSoftmax, 5)));
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[32];
@@ -372,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.ds_full());
+      mbar_arrive(bars.do_empty(ds));  // D_i has been read
     }
     // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled)
     if (ok && any)
