@@ -61,8 +61,8 @@ struct FwdLayout {
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
   static constexpr int kListOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], teardown
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2][2], o_done[2], teardown
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 4 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 32;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
@@ -81,7 +81,8 @@ struct Bars {
   __device__ uint32_t kv_full(int s) const { return base + 8 * (1 + s); }
   __device__ uint32_t kv_empty(int s) const { return base + 8 * (1 + stages + s); }
   __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 2 * stages + t); }
-  __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 2 * stages + t); }
+  // P_t for keys 64u .. 64u + 63 is in tensor memory (and O_t rescaled)
+  __device__ uint32_t p_full(int t, int u) const { return base + 8 * ((u ? 8 : 3) + 2 * stages + t); }
   __device__ uint32_t o_done(int t) const { return base + 8 * (5 + 2 * stages + t); }
   __device__ uint32_t teardown() const { return base + 8 * (7 + 2 * stages); }
 };
@@ -140,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars.s_full(t), 1);
-      mbar_init(bars.p_full(t), 128);
+      mbar_init(bars.p_full(t, 0), 128);
+      mbar_init(bars.p_full(t, 1), 128);
     }
     for (int t = 0; t < 2; ++t) mbar_init(bars.o_done(t), 1);
     mbar_init(bars.teardown(), 1);
@@ -303,10 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       // B = V with keys as K (MN-major, 16 key rows per step). With d = 128,
       // S_t(n+1) is issued after this MMA into the columns P_t occupies; MMAs
       // issued by one thread execute in issue order, so P_t is read first.
-      auto issue_pv = [&](int t, int vslot, bool first) {
+      // (keys 64u .. 64u + 63: half u of P_t)
+      auto issue_pv = [&](int t, int vslot, bool first, int u) {
         const uint32_t v_base = sKV + vslot * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
+        for (int kk = 4 * u; kk < 4 * u + 4; ++kk)
           mma_f16kind_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
                       sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
                       (kk > 0 || !first) ? 1u : 0u);
@@ -341,12 +344,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (entry_act(e, t)) {
-            ok = mbar_wait(bars.p_full(t), pcount[t] & 1u, st,
-                           status_code(kKernFwd, kRoleMma, 5 + t));
+            // PV_t in two halves: the first runs while the softmax warps
+            // form the second half of P_t (the split-key instantiation waits
+            // for all of P_t on p_full(t, 1))
+            if constexpr (!kSplit) {
+              ok = mbar_wait(bars.p_full(t, 0), pcount[t] & 1u, st,
+                             status_code(kKernFwd, kRoleMma, 5 + t));
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, vslot, first_pv[t], 0);
+            }
+            ok = mbar_wait(bars.p_full(t, 1), pcount[t] & 1u, st,
+                           status_code(kKernFwd, kRoleMma, 9 + t));
             if (!ok) break;
             ++pcount[t];
             tc_fence_after();
-            issue_pv(t, vslot, first_pv[t]);
+            if constexpr (kSplit) issue_pv(t, vslot, first_pv[t], 0);
+            issue_pv(t, vslot, first_pv[t], 1);
             first_pv[t] = false;
             // O_t is final once this entry's PV has completed: under causal
             // masking Q tile 0 usually ends one K/V tile before Q tile 1, and
@@ -418,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           m_used = m_tile;
         }
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+        // (the split-key instantiation announces all of P_t at once: the
+        // early announcement costs it spills at the register limit)
+        const bool resc = kSplit || (any && __any_sync(0xffffffffu, need));
         // P = exp2(s*c - m) -> 16-bit pairs (keys 2x, 2x+1 in column x) in tensor
         // memory; the row sum uses 4 independent partial sums
         float lp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -430,6 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           pk0[x] = pack2<kF16>(p0, p1);
         }
         tmem_st32(tP, pk0);
+        // keys 0..63 of P_t go to the MMA now, unless this warp's rows must
+        // first rescale O_t (then both halves are announced below); the
+        // barrier of this warpgroup's tile from threadIdx (fewer live registers)
+        if (!resc) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bars.p_full(0, 0) + ((~threadIdx.x & 128u) >> 4));
+        }
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         tmem_st32(tP + 32, pk1);
         l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
-        if (any && __any_sync(0xffffffffu, need)) {
+        if (resc && any && __any_sync(0xffffffffu, need)) {
           // O *= alpha for this row. The PV MMA of the previous tile has
           // completed: it was issued before this S tile, whose completion we
           // waited for.
@@ -455,7 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         tmem_wait_st();  // P (and a rescaled O) are in tensor memory
         tc_fence_before();
-        mbar_arrive(bars.p_full(t));
+        if (resc && !kSplit) mbar_arrive(bars.p_full(0, 0) + ((~threadIdx.x & 128u) >> 4));
+        if constexpr (kSplit)
+          mbar_arrive(bars.p_full(t, 1));
+        else
+          mbar_arrive(bars.p_full(0, 1) + ((~threadIdx.x & 128u) >> 4));
         any = true;
       }
       // epilogue: O / l and LSE
