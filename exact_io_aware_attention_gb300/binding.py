@@ -190,7 +190,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
 
     q is [B, H, Nq, d], k and v [B, H, Nk, d], all bf16 or all fp16, with any
     strides over the first three dimensions (e.g. permuted views of
-    [B, N, H, d] tensors); d is 64, 96 or 128. O has q's shape and, unless
+    [B, N, H, d] tensors); d is 64, 96, 128 or 256. O has q's shape and, unless
     ``out`` is given, q's layout and dtype (or ``o_dtype=torch.float32``);
     LSE is fp32 contiguous [B, H, Nq]. With ``causal``, query i sees key j
     iff j <= i + Nk - Nq.
