@@ -49,8 +49,8 @@ struct DqLayout {
   static constexpr int kListOff = kVOff + kVSlots * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
   // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full, s_free,
-  // dp_full, ds_full[2], dq_step[2], dq_final, teardown, dp_free
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 10;
+  // dp_full, ds_full[2][2], dq_step[2], dq_final, teardown, dp_free
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 12;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -67,7 +67,10 @@ struct Bars {
   __device__ uint32_t s_full() const { return base + 8 * 11; }
   __device__ uint32_t s_free() const { return base + 8 * 12; }
   __device__ uint32_t dp_full() const { return base + 8 * 13; }
-  __device__ uint32_t ds_full(int b) const { return base + 8 * (b ? 18 : 14); }
+  // dS buffer b holds keys 64h + 32u .. 64h + 32u + 31 of both warpgroups h
+  __device__ uint32_t ds_full(int b, int u) const {
+    return base + 8 * (u ? 21 + b : (b ? 18 : 14));
+  }
   __device__ uint32_t dq_step(int b) const { return base + 8 * (b ? 19 : 15); }
   __device__ uint32_t dq_final() const { return base + 8 * 16; }
   __device__ uint32_t teardown() const { return base + 8 * 17; }
@@ -132,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     mbar_init(bars.s_free(), 256);
     mbar_init(bars.dp_full(), 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars.ds_full(b), 256);
+      mbar_init(bars.ds_full(b, 0), 256);
+      mbar_init(bars.ds_full(b, 1), 256);
       mbar_init(bars.dq_step(b), 1);
     }
     mbar_init(bars.dp_free(), 256);
@@ -301,15 +305,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
           mma_commit(bars.v_empty(vs));
         }
         const int b = n & 1;
-        ok = mbar_wait(bars.ds_full(b), (n >> 1) & 1, st, status_code(kKernBwdDq, kRoleMma, 6));
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t kb = sK + ks * L::kTileBytes;
+        // dQ(n) in the two halves of dS(n): the first runs while the softmax
+        // warps form the second
+        for (int u = 0; u < 2 && ok; ++u) {
+          ok = mbar_wait(bars.ds_full(b, u), (n >> 1) & 1, st,
+                         status_code(kKernBwdDq, kRoleMma, u ? 10 : 6));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16kind_ts(tmem + L::kColDQ, tmem + L::kColDS + 64 * b + kk * 8,
-                      sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024), kIdDq,
-                      (n > 0 || kk > 0) ? 1u : 0u);
+          for (int e = 0; e < 4; ++e) {
+            const int kk = (e >> 1) * 4 + 2 * u + (e & 1);
+            mma_f16kind_ts(tmem + L::kColDQ, tmem + L::kColDS + 64 * b + kk * 8,
+                        sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024), kIdDq,
+                        (n > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
         mma_commit(bars.dq_step(b));
         mma_commit(bars.k_empty(ks));
       }
@@ -360,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
                                              status_code(kKernBwdDq, kRoleSoftmax, 2)));
       if (!ok) break;
       tc_fence_after();
-      uint32_t dsp[32];  // dS as packed 16-bit pairs: keys (2x, 2x+1) of this half
+      const int b = n & 1;
       {
         uint32_t dr[2][32];
         tmem_ld32(t + L::kColDP + 64 * h, dr[0]);
@@ -368,22 +380,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bars.dp_free());
+        // dS as packed 16-bit pairs (keys 2x, 2x+1 of this half), in two
+        // halves of 32 keys, each announced on its own barrier
 #pragma unroll
-        for (int x = 0; x < 64; x += 2)
-          dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x >> 5][x & 31]) - dd),
-                                   pr[x + 1] * (__uint_as_float(dr[x >> 5][(x + 1) & 31]) - dd));
+        for (int u = 0; u < 2; ++u) {
+          uint32_t dsp[16];
+#pragma unroll
+          for (int x = 0; x < 32; x += 2)
+            dsp[x / 2] = pack2<kF16>(pr[32 * u + x] * (__uint_as_float(dr[u][x]) - dd),
+                                     pr[32 * u + x + 1] * (__uint_as_float(dr[u][x + 1]) - dd));
+          if (u == 0 && n >= 2) {
+            // buffer b is free once the dQ MMAs of step n - 2 have read it
+            ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_step(b), ((n >> 1) + 1) & 1, st,
+                                                   status_code(kKernBwdDq, kRoleSoftmax, 3)));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st16(t + L::kColDS + 64 * b + 32 * h + 16 * u, dsp);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bars.ds_full(b, u));
+        }
       }
-      const int b = n & 1;
-      if (n >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.dq_step(b), ((n >> 1) + 1) & 1, st,
-                                               status_code(kKernBwdDq, kRoleSoftmax, 3)));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      tmem_st32(t + L::kColDS + 64 * b + 32 * h, dsp);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.ds_full(b));
+      if (!ok) break;
     }
     // epilogue: dQ = scale * accumulator, this half of the d columns
     if (ok && count > 0)
