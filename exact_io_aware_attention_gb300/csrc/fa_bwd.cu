@@ -245,14 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
         ++ndo;
       }
       // teardown: every copy issued has landed
-      mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleLoad, 2));
+      mbar_wait_drain(bars.kv_full(), 0, st, status_code(kKernBwd, kRoleLoad, 2));
       for (int s = 0; s < L::kQSlots && s < nq; ++s) {
         const int last = s + ((nq - 1 - s) / L::kQSlots) * L::kQSlots;
-        mbar_wait(bars.q_full(s), (last / L::kQSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 3));
+        mbar_wait_drain(bars.q_full(s), (last / L::kQSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 3));
       }
       for (int s = 0; s < L::kdOSlots && s < ndo; ++s) {
         const int last = s + ((ndo - 1 - s) / L::kdOSlots) * L::kdOSlots;
-        mbar_wait(bars.do_full(s), (last / L::kdOSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 5));
+        mbar_wait_drain(bars.do_full(s), (last / L::kdOSlots) & 1u, st, status_code(kKernBwd, kRoleLoad, 5));
       }
     }
     __syncwarp();
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
       }
       if (ok) mma_commit(bars.acc_done());
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKernBwd, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernBwd, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {

@@ -283,14 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
         }
       }
       // teardown: every copy issued has landed
-      mbar_wait(bars.k_full(), 0, st, status_code(kKernBwd256Dv, kRoleLoad, 3));
+      mbar_wait_drain(bars.k_full(), 0, st, status_code(kKernBwd256Dv, kRoleLoad, 3));
       for (int s = 0; s < L::kSlots && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / L::kSlots) * L::kSlots;
-        mbar_wait(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKernBwd256Dv, kRoleLoad, 4));
+        mbar_wait_drain(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKernBwd256Dv, kRoleLoad, 4));
       }
       for (int b = 0; b < 2 && b < nst; ++b) {
         const int last = b + ((nst - 1 - b) / 2) * 2;
-        mbar_wait(bars.stat_full(b), (last >> 1) & 1u, st, status_code(kKernBwd256Dv, kRoleLoad, 5));
+        mbar_wait_drain(bars.stat_full(b), (last >> 1) & 1u, st, status_code(kKernBwd256Dv, kRoleLoad, 5));
       }
     }
     __syncwarp();
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_dv(const __grid_constan
       }
       if (ok && any) mma_commit(bars.acc_done());
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKernBwd256Dv, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernBwd256Dv, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -632,14 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
         x = xn;
       }
       // teardown: every copy issued has landed
-      mbar_wait(bars.a_full(), 0, st, status_code(kKern, kRoleLoad, 3));
+      mbar_wait_drain(bars.a_full(), 0, st, status_code(kKern, kRoleLoad, 3));
       for (int s = 0; s < L::kSlots && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / L::kSlots) * L::kSlots;
-        mbar_wait(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKern, kRoleLoad, 4));
+        mbar_wait_drain(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKern, kRoleLoad, 4));
       }
       for (int b = 0; b < 2 && b < nst; ++b) {
         const int last = b + ((nst - 1 - b) / 2) * 2;
-        mbar_wait(bars.stat_full(b), (last >> 1) & 1u, st, status_code(kKern, kRoleLoad, 5));
+        mbar_wait_drain(bars.stat_full(b), (last >> 1) & 1u, st, status_code(kKern, kRoleLoad, 5));
       }
     }
     __syncwarp();
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd256_grad(const __grid_const
       }
       if (ok && any) mma_commit(bars.acc_done());
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKern, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKern, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {

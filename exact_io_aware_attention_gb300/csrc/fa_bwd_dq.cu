@@ -239,14 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         if (ok) load_v(n);
       }
       // teardown: every copy issued has landed
-      mbar_wait(bars.q_full(), 0, st, status_code(kKernBwdDq, kRoleLoad, 3));
+      mbar_wait_drain(bars.q_full(), 0, st, status_code(kKernBwdDq, kRoleLoad, 3));
       for (int s = 0; s < L::kKSlots && s < nk; ++s) {
         const int last = s + ((nk - 1 - s) / L::kKSlots) * L::kKSlots;
-        mbar_wait(bars.k_full(s), (last / L::kKSlots) & 1u, st, status_code(kKernBwdDq, kRoleLoad, 4));
+        mbar_wait_drain(bars.k_full(s), (last / L::kKSlots) & 1u, st, status_code(kKernBwdDq, kRoleLoad, 4));
       }
       for (int s = 0; s < L::kVSlots && s < nv; ++s) {
         const int last = s + ((nv - 1 - s) / L::kVSlots) * L::kVSlots;
-        mbar_wait(bars.v_full(s), (last / L::kVSlots) & 1u, st, status_code(kKernBwdDq, kRoleLoad, 5));
+        mbar_wait_drain(bars.v_full(s), (last / L::kVSlots) & 1u, st, status_code(kKernBwdDq, kRoleLoad, 5));
       }
     }
     __syncwarp();
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       }
       if (ok && count > 0) mma_commit(bars.dq_final());
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKernBwdDq, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernBwdDq, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {

@@ -104,6 +104,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, StatusS
   return mbar_wait_slow(bar, parity, st, code);
 }
 
+// Teardown wait for copies and MMAs this CTA has already issued. Unlike
+// mbar_wait it keeps waiting after another role of the CTA has given up:
+// work in flight still writes this CTA's shared and tensor memory, so the CTA
+// must not free its tensor memory or exit before that work is done. Only its
+// own time limit ends it (recording `code` if no earlier failure did).
+static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, StatusSlot st,
+                                                    uint32_t code) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && global_timer_ns() - t0 > st.limit_ns) {
+      *(volatile int *)st.abort_flag = 1;
+      if (st.word) atomicCAS(st.word, 0u, code);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies)
 
