@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t sKV = s_base + L::kKVOff;
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kListOff);
   // [0] tmem base [1] count [2] abort [3] ring positions loaded in set-up
-  // [4], [5] last list entry of Q tile 0 / 1
+  // [4], [5] last list entry of Q tile 0 / 1 [6] head b * H + h (for the epilogue)
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
   Bars bars{s_base + L::kBarOff, L::kStages};
   StatusSlot st{p.status, &misc[2], p.wait_limit_ns};
@@ -119,15 +119,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work item: heavy (late) Q-tile pairs first across all heads; the splits
-  // of one pair are adjacent, so they run together and share Q in L2
+  // work item: head groups, heavy (late) Q-tile pairs first within a group;
+  // the splits of one pair are adjacent, so they run together and share Q in L2
   const Shape &sh = p.sh;
   const int npairs = (sh.tq + 1) >> 1;
   const int n_split = kSplit ? p.n_split : 1;
   const int split = kSplit ? int(blockIdx.x % n_split) : 0;
   const int cta = kSplit ? int(blockIdx.x / n_split) : int(blockIdx.x);
-  const int bh = cta % sh.bh;
-  const int pair = npairs - 1 - cta / sh.bh;
+  int pair;
+  const int bh = fwd_item_head(cta, sh.bh, npairs, p.head_group, &pair);
   const int i0 = 2 * pair;
   const bool has1 = (i0 + 1) < sh.tq;
   const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     for (int t = 0; t < 2; ++t) mbar_init(bars.o_done(t), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
+    misc[6] = bh;
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -273,10 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       // teardown: wait (bounded) until every copy issued has landed (the Q
       // tiles were loaded during set-up)
-      mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+      mbar_wait_drain(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
       for (int s = 0; s < L::kStages && s < pos; ++s) {
         const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
-        mbar_wait(bars.kv_full(s), (last / L::kStages) & 1u, st,
+        mbar_wait_drain(bars.kv_full(s), (last / L::kStages) & 1u, st,
                   status_code(kKernFwd, kRoleLoad, 3));
       }
     }
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       // teardown: every MMA this thread issued has completed
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -500,9 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tc_fence_after();
         // destination of this row (indices recomputed here: fewer live registers):
         // O itself, or this split's fp32 partial
-        const int bh_e = int((kSplit ? blockIdx.x / p.n_split : blockIdx.x) % sh.bh);
+        const int bh_e = *reinterpret_cast<volatile int *>(&misc[6]);
         constexpr bool to_part = kSplit;
-        const size_t prow = ((size_t)split * sh.bh + bh) * sh.nq + qrow;
+        const size_t prow = ((size_t)split * sh.bh + bh_e) * sh.nq + qrow;
         const size_t row = to_part ? prow * D : p.so.row(bh_e / sh.heads, bh_e % sh.heads, qrow);
         float *const o32 = to_part ? p.o_part : static_cast<float *>(p.o);
         const float inv_l = (any && l > 0.f) ? 1.f / l : 0.f;
@@ -548,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         // LSE = ln(sum_j exp(scale s_ij)) = ln2 * (m + log2 l)
         if (live)
-          (to_part ? p.lse_part[prow] : p.lse[(size_t)bh * sh.nq + qrow]) =
+          (to_part ? p.lse_part[prow] : p.lse[(size_t)bh_e * sh.nq + qrow]) =
               (any && l > 0.f) ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
 
       }

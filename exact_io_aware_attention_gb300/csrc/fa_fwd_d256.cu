@@ -92,13 +92,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work item: heavy (late) Q tiles first across all heads; splits adjacent
+  // work item: head groups, heavy (late) Q tiles first within a group; splits adjacent
   const Shape &sh = p.sh;
   const int n_split = kSplit ? p.n_split : 1;
   const int split = kSplit ? int(blockIdx.x % n_split) : 0;
   const int cta = kSplit ? int(blockIdx.x / n_split) : int(blockIdx.x);
-  const int bh = cta % sh.bh;
-  const int i = sh.tq - 1 - cta / sh.bh;  // Q tile
+  int i;  // Q tile
+  const int bh = fwd_item_head(cta, sh.bh, sh.tq, p.head_group, &i);
   const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
 
   // ---- setup -------------------------------------------------------------
@@ -214,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
         for (int h = 0; h < 2 && ok; ++h) load_half(&p.tm_v, n, h);
       }
       // teardown: every copy issued has landed
-      mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+      mbar_wait_drain(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
       for (int s = 0; s < L::kSlots && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / L::kSlots) * L::kSlots;
-        mbar_wait(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKernFwd, kRoleLoad, 3));
+        mbar_wait_drain(bars.full(s), (last / L::kSlots) & 1u, st, status_code(kKernFwd, kRoleLoad, 3));
       }
     }
     __syncwarp();
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
       if (ok && count > 0) mma_commit(bars.o_done());
       // teardown: every MMA this thread issued has completed
       mma_commit(bars.teardown());
-      mbar_wait(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
+      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
     }
     __syncwarp();
   } else if (warp >= 4) {

@@ -65,6 +65,20 @@ struct Shape {
   }
 };
 
+// Work order of a forward grid: item `cta` (0 .. units*bh - 1; the split
+// CTAs of one item share it) runs unit `*unit` (a Q-tile pair, or a Q tile)
+// of head `bh`. Heads go in groups of `hg`; within a group the heavy units
+// (late Q tiles under causal masking) come first, so the CTAs in flight at
+// any time cover only a few heads and those heads' K and V stay in L2.
+__host__ __device__ inline int fwd_item_head(int cta, int bh, int units, int hg, int *unit) {
+  const int group = cta / (hg * units);
+  const int g_base = group * hg;
+  const int g_size = min(hg, bh - g_base);
+  const int g_rank = cta - group * hg * units;
+  *unit = units - 1 - g_rank / g_size;
+  return g_base + g_rank % g_size;
+}
+
 struct FwdParams {
   // 4-D maps over [B][H][rows][d] (dims d, rows, H, B) of bf16 or f16 elements,
   // box 64 x 128 x 1 x 1, 128-byte swizzle; rows past the end of a head and
@@ -85,6 +99,7 @@ struct FwdParams {
   unsigned int *status;               // device status word
   uint32_t debug_flags;               // kDebug* bits (tests of the failure path only)
   uint64_t wait_limit_ns;             // limit of one kernel-side wait
+  int head_group;                     // CTA order: heads per group (1..bh), fwd_item_head
 };
 
 struct BwdParams {
