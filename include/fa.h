@@ -32,7 +32,10 @@
  *    caller. The library never allocates, frees or synchronises; all work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *    default stream), which must belong to the device that holds Q. Each call
- *    makes that device current on the calling thread. Inputs are only read;
+ *    makes that device current on the calling thread and leaves it current
+ *    on return (the caller's previous current device is not restored; a
+ *    caller that drives several devices from one thread sets its own device
+ *    again after the call). Inputs are only read;
  *    outputs must not overlap one another or an input.
  *  - Supported: d in {64, 96, 128, 256}; 1 <= Nq, Nk <= 65536 (any length: a last,
  *    partial tile of 128 rows is handled inside the kernels); B, H >= 1;
@@ -230,11 +233,14 @@ fa_status fa_backward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor
  * allocates no memory (no cudaMalloc, no cudaFree, no allocating library
  * routine) as long as the measurement hooks are off, which is the default.
  *
- * The first call on a device looks up the scratch area's device address on
- * that device; make that first call before any stream capture. All calls on
- * a device share the one area, and it keeps the last call's contents (each
- * call re-initialises what must start at zero itself). Calls that overlap
- * on the GPU, e.g. on two streams at once, race on the area: serialise them.
+ * Every call looks up the scratch area's device address on the device that
+ * holds Q (cudaGetSymbolAddress; the first such lookup on a device loads the
+ * library's device code there). Make the first call on a device before any
+ * stream capture. All calls on a device share the one area, and it keeps the
+ * last call's contents (each call re-initialises what must start at zero
+ * itself). Calls that overlap on the GPU, e.g. on two streams at once, race
+ * on the area: serialise them. Like every entry point, the call leaves the
+ * device that holds Q current on the calling thread.
  */
 fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const void *O,
                               const void *dO, const float *LSE, void *dQ, void *dK, void *dV,

@@ -102,8 +102,7 @@ def test_autograd_wrapper_matches_backward():
     out = fa().attention(qg, kg, vg, causal=True)
     out.backward(do)
     dq, dk, dv = run_fwd_bwd(inp, True, None, None)
-    assert torch.equal(qg.grad, dq) or (qg.grad.float() - dq.float()).abs().max() < 1e-2
-    assert torch.equal(kg.grad, dk) and torch.equal(vg.grad, dv)
+    assert torch.equal(qg.grad, dq) and torch.equal(kg.grad, dk) and torch.equal(vg.grad, dv)
 
 
 EDGE_ROWS = (0, 1, 2, 127, 128, 129)
