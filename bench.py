@@ -141,7 +141,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, timed_ms=None):
         rows = []
         try:
             with open(self.path) as f:
@@ -154,21 +154,34 @@ class ClockSampler:
         finally:
             if self.path and os.path.exists(self.path):
                 os.unlink(self.path)
-        return summarize_clocks(rows)
+        return summarize_clocks(rows, timed_ms, self.period)
 
 
-def summarize_clocks(rows):
+LOAD_WATTS = 300.0  # a sample counts as "under load" above this board power
+
+
+def summarize_clocks(rows, timed_ms=None, period_ms=None):
+    """Clock record of the samples taken around the timed region. Only samples
+    above LOAD_WATTS count as under load; when none is (a timed region shorter
+    than the sampling period can fall between samples), sm_mhz is the median
+    of all samples and sm_mhz_basis says so."""
     if not rows:
-        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                "samples_under_load": 0, "timed_region_ms": timed_ms,
+                "sample_period_ms": period_ms}
     sm = [int(r[1]) for r in rows]
     mx = max(int(r[2]) for r in rows)
     power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
-    busy = [s for s, r in zip(sm, rows) if float(r[3] or 0) > 300.0] or sm
+    busy = [s for s, r in zip(sm, rows)
+            if r[3].replace(".", "", 1).isdigit() and float(r[3]) > LOAD_WATTS]
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
-    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": reasons,
-            "samples": len(rows), "samples_under_load": len(busy),
-            "power_w_max": max(power) if power else None}
+    return {"sm_mhz": statistics.median(busy if busy else sm), "sm_max_mhz": mx,
+            "sm_mhz_basis": "samples under load" if busy else
+                            f"all samples (none above {LOAD_WATTS:.0f} W)",
+            "reasons": reasons, "samples": len(rows), "samples_under_load": len(busy),
+            "power_w_max": max(power) if power else None,
+            "timed_region_ms": timed_ms, "sample_period_ms": period_ms}
 
 
 # Source files each measured kernel is compiled from (its own file and the
@@ -308,7 +321,7 @@ def run_cuda(args, dist: Dist):
     fa.profile_enable(False)
     ms_total = e0.elapsed_time(e1)
     per_kernel = fa.profile_collect()
-    clk = clocks.summary()
+    clk = clocks.summary(round(ms_total, 3))
     if fa.device_status() != 0:
         raise RuntimeError("a kernel-side wait gave up in the timed region")
 

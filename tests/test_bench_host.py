@@ -38,11 +38,27 @@ def test_clock_summary():
              "Active"],
             ["0", "345", "2070", "120.0", "0x1", "Not Active", "Not Active", "Not Active",
              "Not Active"]]
-    s = bench.summarize_clocks(rows)
+    s = bench.summarize_clocks(rows, timed_ms=18.3, period_ms=50)
     assert s["sm_max_mhz"] == 2070 and s["samples"] == 3 and s["samples_under_load"] == 2
-    assert s["sm_mhz"] == (2070 + 1980) / 2
+    assert s["sm_mhz"] == (2070 + 1980) / 2 and s["sm_mhz_basis"] == "samples under load"
     assert s["reasons"] == ["sw_power_cap"]
-    assert bench.summarize_clocks([])["samples"] == 0
+    assert s["timed_region_ms"] == 18.3 and s["sample_period_ms"] == 50
+    empty = bench.summarize_clocks([])
+    assert empty["samples"] == 0 and empty["samples_under_load"] == 0
+
+
+def test_clock_summary_without_load_samples():
+    """No sample above the load threshold: nothing is counted as under load."""
+    idle = [["0", "2070", "2070", "165.3", "0x0", "Not Active", "Not Active", "Not Active",
+             "Not Active"],
+            ["0", "1965", "2070", "150.0", "0x0", "Not Active", "Not Active", "Not Active",
+             "Not Active"],
+            ["0", "2055", "2070", "[N/A]", "0x0", "Not Active", "Not Active", "Not Active",
+             "Not Active"]]
+    s = bench.summarize_clocks(idle, timed_ms=18.0, period_ms=50)
+    assert s["samples"] == 3 and s["samples_under_load"] == 0
+    assert s["sm_mhz"] == 2055 and s["sm_mhz_basis"].startswith("all samples")
+    assert s["power_w_max"] == 165.3
 
 
 def test_oracle_sample_step_credits_visible_keys():
