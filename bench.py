@@ -50,6 +50,8 @@ def parse_args(argv=None):
                     help="workload name (profiling runs; the benchmark uses the default)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (profiling runs only)")
+    ap.add_argument("--bwd-algo", choices=["auto", "fused", "split"], default="auto",
+                    help="backward form (A/B runs): one-pass kernel or two-kernel recompute")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -190,6 +192,7 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
     "fa_bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
     "fa_bwd_dq": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
+    "fa_bwd_fused": ("fa_bwd_fused.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
 }
 
 
@@ -284,7 +287,8 @@ def run_cuda(args, dist: Dist):
     o = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
-    ws = torch.empty(fa.backward_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
+    ws = torch.empty(fa.backward_workspace_bytes(*shape, algo=args.bwd_algo), dtype=torch.uint8,
+                     device=dev)
     stream = torch.cuda.current_stream(dev)
     mask = host["mask"].to(dev) if host["mask"] is not None else None
     density = float(host["mask"].float().mean()) if host["mask"] is not None else 1.0
@@ -333,16 +337,21 @@ def run_cuda(args, dist: Dist):
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
     fwd_ms = per_kernel["fa_fwd_kernel"][0] / max(1, per_kernel["fa_fwd_kernel"][1])
-    bwd_parts = ["fa_bwd_pre", "fa_bwd_dkdv", "fa_bwd_dq"]
-    bwd_ms = sum(per_kernel[k][0] for k in bwd_parts) / max(1, per_kernel["fa_bwd_dkdv"][1])
+    # one backward = the preprocess, then either the one-pass kernel and the
+    # dQ conversion or the dK/dV and dQ kernels
+    bwd_parts = ["fa_bwd_pre", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_fused", "fa_bwd_dq_convert"]
+    bwd_ms = sum(per_kernel[k][0] for k in bwd_parts) / max(1, per_kernel["fa_bwd_pre"][1])
+    bwd_form = "one-pass" if per_kernel["fa_bwd_fused"][1] else "two-kernel"
     avg = lambda kname: per_kernel[kname][0] / max(1, per_kernel[kname][1])
     launches = sum(n for _, n in per_kernel.values())
     dominant = max(per_kernel, key=lambda kname: per_kernel[kname][0])
     dom_ms, dom_n = per_kernel[dominant]
-    # the method's GEMMs each kernel performs: the forward's two; dK/dV runs four
-    # of the backward's five (S^T, dP^T, dV, dK); the dQ kernel runs the fifth
-    # (dQ) and recomputes S and dP, which is not credited
-    alg_flops = {"fa_fwd_kernel": fwd_fl, "fa_bwd_dkdv": 0.8 * bwd_fl, "fa_bwd_dq": 0.2 * bwd_fl}
+    # the method's GEMMs each kernel performs: the forward's two; the one-pass
+    # backward all five of the backward's; in the two-kernel form dK/dV runs
+    # four (S^T, dP^T, dV, dK) and the dQ kernel the fifth (dQ), recomputing S
+    # and dP, which is not credited
+    alg_flops = {"fa_fwd_kernel": fwd_fl, "fa_bwd_fused": bwd_fl, "fa_bwd_dkdv": 0.8 * bwd_fl,
+                 "fa_bwd_dq": 0.2 * bwd_fl}
     dom_flops = alg_flops.get(dominant, 0.0)
     achieved = dom_flops / (dom_ms / dom_n * 1e-3) / 1e12 if dom_n else 0.0
 
@@ -411,7 +420,8 @@ def run_cuda(args, dist: Dist):
 
     # ---- secondary ceilings: the exponential rate and HBM bytes ---------------
     # One exp per visible score element in the forward (4 d flops each); the
-    # backward recomputes P in both of its kernels (2 exps per element).
+    # one-pass backward recomputes P once (1 exp per element), the two-kernel
+    # form in both of its kernels (2).
     # Algorithmic bytes per head: forward reads Q, K, V and writes O (16-bit)
     # and LSE; backward reads Q, K, V, O, dO and LSE, writes dQ, dK, dV, and
     # writes and reads D and LSE*log2(e).
@@ -422,12 +432,17 @@ def run_cuda(args, dist: Dist):
     heads = w.B * w.H
     fwd_bytes = heads * ((3 * 2 + 2) * w.N * w.d + 4 * w.N)
     bwd_bytes = heads * ((5 * 2 + 3 * 2) * w.N * w.d + 4 * w.N + 16 * w.N)
+    # the one-pass form zeroes its fp32 dQ accumulator, writes it back from L2
+    # and reads it once more to convert it
+    if bwd_form == "one-pass":
+        bwd_bytes += heads * 3 * 4 * w.N * w.d
+    bwd_exp_per_elem = 1 if bwd_form == "one-pass" else 2  # P recomputed once or twice
     sfu = {"exp2_ops_per_clk_per_sm": round(peak_exps / sms / (mhz * 1e6), 2),
            "peak_exps_per_s": peak_exps,
            "fwd_exps_per_s": fwd_exps / (fwd_ms * 1e-3),
            "fwd_frac": round(fwd_exps / (fwd_ms * 1e-3) / peak_exps, 4),
-           "bwd_exps_per_s_executed": 2 * fwd_exps / (bwd_ms * 1e-3),
-           "bwd_frac": round(2 * fwd_exps / (bwd_ms * 1e-3) / peak_exps, 4),
+           "bwd_exps_per_s_executed": bwd_exp_per_elem * fwd_exps / (bwd_ms * 1e-3),
+           "bwd_frac": round(bwd_exp_per_elem * fwd_exps / (bwd_ms * 1e-3) / peak_exps, 4),
            "clock_mhz": mhz}
     hbm = {"fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1),
            "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1),
@@ -455,11 +470,14 @@ def run_cuda(args, dist: Dist):
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_fl / fwd_ms / 1e9, 1),
                 "frac_of_peak": round(fwd_fl / fwd_ms / 1e9 / peak, 4)},
         "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_fl / bwd_ms / 1e9, 1),
-                "frac_of_peak": round(bwd_fl / bwd_ms / 1e9 / peak, 4),
-                "dkdv_kernel_ms": round(avg("fa_bwd_dkdv"), 4),
-                "dq_kernel_ms": round(avg("fa_bwd_dq"), 4),
-                "dq_kernel_executed_tflops": round(0.6 * bwd_fl / avg("fa_bwd_dq") / 1e9, 1)
-                if per_kernel["fa_bwd_dq"][1] else None},
+                "frac_of_peak": round(bwd_fl / bwd_ms / 1e9 / peak, 4), "form": bwd_form,
+                **({"fused_kernel_ms": round(avg("fa_bwd_fused"), 4),
+                    "dq_convert_ms": round(avg("fa_bwd_dq_convert"), 4)}
+                   if bwd_form == "one-pass" else
+                   {"dkdv_kernel_ms": round(avg("fa_bwd_dkdv"), 4),
+                    "dq_kernel_ms": round(avg("fa_bwd_dq"), 4),
+                    "dq_kernel_executed_tflops": round(0.6 * bwd_fl / avg("fa_bwd_dq") / 1e9, 1)}),
+                "pre_ms": round(avg("fa_bwd_pre"), 4)},
         "per_kernel_ms": {kname: round(t / n, 4) for kname, (t, n) in per_kernel.items() if n},
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),

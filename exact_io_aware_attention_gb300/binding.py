@@ -48,6 +48,7 @@ SIGNATURES = {
     "fa_forward_split_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "fa_forward_num_splits": ([_i, _i, _i, _i, _i, _i], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "fa_backward_min_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "fa_backward_ex": ([_tp] * 5 + [_vp] + [_tp] * 3 +
                        [_i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
@@ -230,24 +231,33 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
     return out, lse
 
 
-def backward_workspace_bytes(B, H, N, d) -> int:
-    """Workspace bytes of the backward pass for N query rows per (batch, head)."""
+def backward_workspace_bytes(B, H, N, d, algo: str = "auto") -> int:
+    """Workspace bytes of the backward pass for N query rows per (batch, head):
+    enough for the one-pass kernel ("auto", "fused"), or the row statistics
+    only, which selects the two-kernel form ("split")."""
+    if algo == "split":
+        return int(_lib_fast().fa_backward_min_workspace_bytes(B, H, N, d))
+    if algo not in ("auto", "fused"):
+        raise ValueError(f"algo must be 'auto', 'fused' or 'split', not {algo!r}")
     return int(_lib_fast().fa_backward_workspace_bytes(B, H, N, d))
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
-             block_mask=None, workspace=None, dq=None, dk=None, dv=None):
+             block_mask=None, workspace=None, dq=None, dk=None, dv=None, algo: str = "auto"):
     """dQ, dK, dV of attention for upstream gradient ``do``.
 
     Shapes and layouts as in ``forward``: q, o, do, dq are [B, H, Nq, d], k, v,
     dk, dv [B, H, Nk, d], all bf16 or all fp16, with any strides over the
     first three dimensions; each gradient takes its input's layout unless
-    given.
+    given. ``algo`` sizes the workspace when none is given: "auto"/"fused"
+    for the one-pass backward (head dimensions up to 128; dQ accumulated with
+    atomic adds), "split" for the two-kernel form (bitwise reproducible). A
+    given ``workspace`` decides by its size, as fa_backward_ex does.
     """
     B, H, Nq, Nk, d = _shapes(q, (k, v), (o, do))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     mask = _mask(block_mask, Nq, Nk)
-    nbytes = backward_workspace_bytes(B, H, Nq, d)
+    nbytes = backward_workspace_bytes(B, H, Nq, d, algo)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq

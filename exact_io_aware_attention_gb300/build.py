@@ -20,7 +20,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_bwd_d256.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_bwd_d256.cu",
+           "fa_bwd_fused.cu"]
 HEADERS = ["ptx.cuh", "fa_internal.h", "tile_store.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -143,6 +143,29 @@ bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, 
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the one-pass backward's fp32 dQ accumulator: `rows` rows of d
+// floats, 32 x 32 boxes (128 bytes wide) in the 128-byte swizzle, for the
+// kernel's TMA tensor reductions.
+bool encode_dq_acc(CUtensorMap *m, float *base, long long rows, int d) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    snprintf(g_last_error, sizeof(g_last_error),
+             "cuTensorMapEncodeTiled(dQ accumulator %p, rows=%lld, d=%d) failed: CUresult %d",
+             (void *)base, rows, d, (int)r);
+  return r == CUDA_SUCCESS;
+}
+
 // Heads per CTA group of the backward grid (kept small so the fp32 dQ rows
 // that concurrent CTAs accumulate stay in L2). FA_BWD_HEAD_GROUP overrides it
 // for tuning runs.
@@ -327,9 +350,31 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   return e == cudaSuccess ? FA_OK : cuda_fail("forward launch", e);
 }
 
-size_t workspace_bytes(int B, int H, int Nq) {
+// Backward workspace: fp32 D and LSE * log2(e) per padded query row (both
+// paths), then, for the one-pass backward (head dimensions up to 128), the fp32
+// dQ accumulator of d floats per padded query row.
+size_t stats_workspace_bytes(int B, int H, int Nq) {
   const size_t rows = (size_t)B * H * (size_t)((Nq + fa::kTile - 1) / fa::kTile) * fa::kTile;
   return 2 * round_up(rows * sizeof(float));
+}
+
+size_t dq_acc_bytes(int B, int H, int Nq, int d) {
+  if (d > 128) return 0;
+  const size_t rows = (size_t)B * H * (size_t)((Nq + fa::kTile - 1) / fa::kTile) * fa::kTile;
+  return round_up(rows * (size_t)d * sizeof(float));
+}
+
+// Whether a backward with this much workspace runs the one-pass kernel: the
+// workspace holds the dQ accumulator too, and FA_BWD_ALGO=split (a tuning and
+// A/B switch) does not ask for the two-kernel backward.
+bool use_one_pass(int B, int H, int Nq, int d, size_t ws_bytes) {
+  if (d > 128) return false;
+  // the accumulator's rows are addressed with 32-bit TMA coordinates
+  if ((long long)B * H * ((Nq + fa::kTile - 1) / fa::kTile) * fa::kTile > 0x7fffffffLL)
+    return false;
+  const char *e = getenv("FA_BWD_ALGO");
+  if (e && strcmp(e, "split") == 0) return false;
+  return ws_bytes >= stats_workspace_bytes(B, H, Nq) + dq_acc_bytes(B, H, Nq, d);
 }
 
 fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *V,
@@ -343,7 +388,7 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
-  if (ws_bytes < workspace_bytes(B, H, Nq)) return FA_ERR_INVALID_ARG;
+  if (ws_bytes < stats_workspace_bytes(B, H, Nq)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   memset(&p, 0, sizeof(p));
   fa::RowStrides sq, sk, sv;
@@ -378,9 +423,15 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   p.o = O->data;
   p.dout = dO->data;
   p.lse = LSE;
-  const size_t stat_bytes = workspace_bytes(B, H, Nq) / 2;
+  const size_t stat_bytes = stats_workspace_bytes(B, H, Nq) / 2;
   p.delta = static_cast<float *>(workspace);
   p.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + stat_bytes);
+  p.dq_acc = use_one_pass(B, H, Nq, d, ws_bytes)
+                 ? reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * stat_bytes)
+                 : nullptr;
+  if (p.dq_acc &&
+      !encode_dq_acc(&p.tm_dqacc, p.dq_acc, (long long)B * H * p.sh.tq * fa::kTile, d))
+    return FA_ERR_CUDA;
   p.dq = dQ->data;
   p.dk = dK->data;
   p.dv = dV->data;
@@ -516,6 +567,8 @@ const char *fa_kernel_name(int kind) {
     case fa::kKindBwd256Dv: return "fa_bwd256_dv";
     case fa::kKindBwd256Dk: return "fa_bwd256_dk";
     case fa::kKindBwd256Dq: return "fa_bwd256_dq";
+    case fa::kKindBwdFused: return "fa_bwd_fused";
+    case fa::kKindBwdConvert: return "fa_bwd_dq_convert";
     default: return "";
   }
 }
@@ -626,7 +679,12 @@ fa_status fa_forward_split_ex(const fa_tensor *Q, const fa_tensor *K, const fa_t
 
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
-  return workspace_bytes(B, H, N);
+  return stats_workspace_bytes(B, H, N) + dq_acc_bytes(B, H, N, d);
+}
+
+size_t fa_backward_min_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
+  return stats_workspace_bytes(B, H, N);
 }
 
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
@@ -715,7 +773,10 @@ fa_status fa_backward_noalloc(const void *Q, const void *K, const void *V, const
   fa_status s = check_shape(B, H, N, N, d, scale, &empty);
   if (s != FA_OK || empty) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
-  const size_t need = fa_backward_workspace_bytes(B, H, N, d);
+  // the one-pass backward when its accumulator fits in the area, else the
+  // two-kernel backward, which needs only the row statistics
+  size_t need = fa_backward_workspace_bytes(B, H, N, d);
+  if (need > kNoAllocScratchBytes) need = fa_backward_min_workspace_bytes(B, H, N, d);
   if (need > kNoAllocScratchBytes) {
     snprintf(g_last_error, sizeof(g_last_error),
              "fa_backward_noalloc: B=%d H=%d N=%d d=%d needs %zu bytes of scratch; the fixed "

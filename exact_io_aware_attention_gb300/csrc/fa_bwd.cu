@@ -13,7 +13,8 @@
 //   dS_ij = P_ij (dP_ij - D_i)
 //   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
 //
-// Three kernels on the caller's stream:
+// The two-kernel backward, three kernels on the caller's stream (the one-pass
+// backward of fa_bwd_fused.cu shares fa_bwd_pre and replaces the other two):
 //   fa_bwd_pre        D_i and LSE_i * log2(e), padded to whole Q tiles
 //   fa_bwd_dkdv       one CTA per 128-key K/V tile, looping over the Q tiles
 //                     that see it (causal: a row of the tile sees one of its
@@ -447,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv(const __grid_constant
 
 // D_i = dO_i . O_i and LSE_i * log2(e) for every row of every Q tile: a row
 // past the end of the sequence, or one that sees no key (LSE = -inf), gets
-// D = 0 and LSE * log2(e) = +inf, which makes its P row exactly 0.
+// D = 0 and LSE * log2(e) = +inf, which makes its P row exactly 0. For the
+// one-pass backward it also zeroes the block's rows of the fp32 dQ
+// accumulator.
 // Block = 64 rows of one head (blockIdx.x = (b * H + h) * chunks + chunk), so
 // the index arithmetic is done once per block; a row is read by 16 threads with
 // 16-byte loads (8 elements each; with a head dimension of 96, run as
@@ -495,6 +498,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre(const __grid_constant__ BwdPar
       p.lse2[stat_head + n] = empty ? INFINITY : l * 1.4426950408889634f;
     }
   }
+  if (p.dq_acc) {  // rows chunk*64 .. chunk*64+63 of the head, sh.d floats each
+    float4 *z = reinterpret_cast<float4 *>(p.dq_acc + (stat_head + (size_t)chunk * kPreRows) * sh.d);
+    const int n4 = kPreRows * sh.d / 4;
+    for (int x = threadIdx.x; x < n4; x += blockDim.x) z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 template <int D, bool kF16>
@@ -512,6 +520,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
   if constexpr (D == 256) {
     return launch_backward_d256(p, stream);  // fa_bwd_d256.cu
   } else {
+    if (p.dq_acc) return launch_backward_fused(p, stream);  // fa_bwd_fused.cu
     using L = DkdvLayout<D>;
     static bool configured = false;
     if (!configured) {

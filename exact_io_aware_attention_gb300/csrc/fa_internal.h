@@ -105,12 +105,16 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
   CUtensorMap tm_dq, tm_dk, tm_dv;     // maps over the gradients, 64 x 32 boxes (TMA stores)
+  CUtensorMap tm_dqacc;                // one-pass backward: 2-D map over dq_acc ([rows][d] fp32),
+                                       // 32 x 32 boxes, 128-byte swizzle (TMA reductions)
   Shape sh;
   const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;
   const float *lse;                   // [B*H][nq]
   float *delta;                       // workspace: D_i, [B*H][tq*128]
   float *lse2;                        // workspace: LSE_i * log2(e), [B*H][tq*128]
+  float *dq_acc;                      // workspace: fp32 dQ accumulator [B*H][tq*128][d] of the
+                                      // one-pass backward (null: the two-kernel backward)
   void *dq, *dk, *dv;                 // 16-bit outputs, strides sdq / sdk / sdv
   RowStrides sdq, sdk, sdv;
   int head_group;                     // CTA order: heads per group (1..bh)
@@ -123,7 +127,8 @@ struct BwdParams {
 // Kernel ids of the measurement hooks (names in fa_kernel_name()).
 enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdDkdv = 2, kKindBwdDq = 3,
                         kKindFwdCombine = 4, kKindBwd256Dv = 5, kKindBwd256Dk = 6,
-                        kKindBwd256Dq = 7, kNumKinds = 8 };
+                        kKindBwd256Dq = 7, kKindBwdFused = 8, kKindBwdConvert = 9,
+                        kNumKinds = 10 };
 
 // Brackets one launch with CUDA events when measurement is enabled
 // (fa_profile_enable); a no-op otherwise.
@@ -144,12 +149,16 @@ cudaError_t launch_forward(const FwdParams &p, cudaStream_t stream);  // + the m
 cudaError_t launch_forward_d256(const FwdParams &p, cudaStream_t stream);  // fa_fwd_d256.cu
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_bwd_dq.cu
+// dK, dV and the dQ partials in one kernel, then the dQ conversion, after
+// fa_bwd_pre has zeroed p.dq_acc; head dimensions 64, 96, 128 (fa_bwd_fused.cu)
+cudaError_t launch_backward_fused(const BwdParams &p, cudaStream_t stream);
 // dV, dK and dQ for head dimension 256, after fa_bwd_pre (fa_bwd_d256.cu)
 cudaError_t launch_backward_d256(const BwdParams &p, cudaStream_t stream);
 
 // Status word codes: 0x80000000 | kernel << 16 | role << 8 | site.
 enum KernelId : uint32_t { kKernFwd = 1, kKernBwdPre = 2, kKernBwd = 3, kKernBwdDq = 4,
-                           kKernBwd256Dv = 5, kKernBwd256Dk = 6, kKernBwd256Dq = 7 };
+                           kKernBwd256Dv = 5, kKernBwd256Dk = 6, kKernBwd256Dq = 7,
+                           kKernBwdFused = 8 };
 __host__ __device__ constexpr uint32_t status_code(uint32_t kernel, uint32_t role, uint32_t site) {
   return 0x80000000u | (kernel << 16) | (role << 8) | site;
 }

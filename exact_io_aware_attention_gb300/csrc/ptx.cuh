@@ -82,8 +82,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase of parity `parity` of barrier `bar` to complete.
 // Returns false (and records `code`) if it gives up or if another role of
 // this CTA already gave up.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, StatusSlot st,
-                                            uint32_t code) {
+__device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, StatusSlot st,
+                                               uint32_t code) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -98,10 +98,24 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// The loop out of line: the callers' hot loops keep their registers.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, StatusSlot st,
+                                                   uint32_t code) {
+  return mbar_wait_loop(bar, parity, st, code);
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, StatusSlot st,
                                           uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, st, code);
+}
+
+// The same wait with the loop inlined, for kernels whose warpgroups set their
+// own register counts (setmaxnreg): there every call is inlined.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, StatusSlot st,
+                                              uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_loop(bar, parity, st, code);
 }
 
 // Teardown wait for copies and MMAs this CTA has already issued. Unlike
@@ -109,8 +123,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, StatusS
 // work in flight still writes this CTA's shared and tensor memory, so the CTA
 // must not free its tensor memory or exit before that work is done. Only its
 // own time limit ends it (recording `code` if no earlier failure did).
-static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, StatusSlot st,
-                                                    uint32_t code) {
+__device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parity, StatusSlot st,
+                                                   uint32_t code) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -120,6 +134,11 @@ static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parit
       return false;
     }
   }
+}
+
+static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, StatusSlot st,
+                                                    uint32_t code) {
+  return mbar_wait_drain_inl(bar, parity, st, code);
 }
 
 // ---------------------------------------------------------------------------

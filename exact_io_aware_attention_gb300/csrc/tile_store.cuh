@@ -20,11 +20,13 @@ namespace fa {
 // `n_rows` stores nothing. With any == false the row is zero.
 //
 // Every thread of the warp must call it (tensor-memory loads are warp-wide),
-// and the buffer at s_tile must be free: no MMA or copy still reads it. It is
-// a function of its own, called once per CTA, so that its registers do not
-// weigh on the kernels' main loops.
+// and the buffer at s_tile must be free: no MMA or copy still reads it.
+// store_rows_tma is a function of its own, called once per CTA, so that its
+// registers do not weigh on the kernels' main loops; store_rows_tma_inl is the
+// same code inlined, for kernels whose warpgroups set their own register
+// counts (setmaxnreg), where every call is inlined.
 template <int kCols, bool kF16>
-__device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc,
+__device__ __forceinline__ void store_rows_tma_inl(const CUtensorMap *tm, uint32_t tacc,
                                             uint32_t s_tile, int r, int tile_row0, int x0,
                                             float sc, bool any, int d_cols, int n_rows,
                                             int h_idx, int b_idx) {
@@ -63,6 +65,15 @@ __device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc
     bulk_wait_group_read0();
   }
   __syncwarp();
+}
+
+template <int kCols, bool kF16>
+__device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc,
+                                            uint32_t s_tile, int r, int tile_row0, int x0,
+                                            float sc, bool any, int d_cols, int n_rows,
+                                            int h_idx, int b_idx) {
+  store_rows_tma_inl<kCols, kF16>(tm, tacc, s_tile, r, tile_row0, x0, sc, any, d_cols, n_rows,
+                                  h_idx, b_idx);
 }
 
 }  // namespace fa

@@ -181,20 +181,42 @@ size_t fa_forward_split_workspace_bytes(int B, int H, int Nq, int d, int num_spl
 int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal);
 
 /*
- * Bytes of device workspace fa_backward and fa_backward_ex need for N query
- * rows per (batch, head): fp32 D (D_i = dO_i.O_i) and fp32 LSE*log2(e), each
- * [B,H,ceil(N/128)*128] and starting on a 256-byte boundary: O(N), 8 bytes
- * per query row. Returns 0 for invalid sizes.
+ * Bytes of device workspace with which fa_backward and fa_backward_ex run the
+ * one-pass backward, for N query rows per (batch, head): fp32 D
+ * (D_i = dO_i.O_i) and fp32 LSE*log2(e), each [B,H,ceil(N/128)*128], then
+ * (d <= 128) an fp32 dQ accumulator [B,H,ceil(N/128)*128,d], each part
+ * starting on a 256-byte boundary: O(N*d), 8 + 4d bytes per query row.
+ * Returns 0 for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * The smallest workspace fa_backward and fa_backward_ex accept: the two
+ * statistics only, 8 bytes per query row (O(N)). With less than
+ * fa_backward_workspace_bytes (or with d = 256) the backward runs the
+ * two-kernel form, which recomputes S and dP in a second kernel that owns dQ
+ * instead of accumulating dQ in the workspace: slower, same results up to
+ * rounding order. Returns 0 for invalid sizes.
+ */
+size_t fa_backward_min_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * Backward pass. Reads Q, K, V, O, dO (bf16) and LSE (fp32, as written by the
  * forward pass with the same arguments); writes dQ, dK, dV (bf16 [B,H,N,d]).
  * `workspace` is a caller-owned device buffer of at least
- * fa_backward_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents
- * on entry do not matter and are clobbered. The score and probability tiles
- * are recomputed on chip and never reach global memory.
+ * fa_backward_min_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its
+ * contents on entry do not matter and are clobbered. The score and
+ * probability tiles are recomputed on chip and never reach global memory.
+ *
+ * With at least fa_backward_workspace_bytes(B,H,N,d) bytes (d <= 128) one
+ * kernel recomputes S and P once per (Q tile, K/V tile) pair and runs all
+ * five products there: dK and dV accumulate on chip, and each pair's dQ
+ * partial is added into the fp32 accumulator in the workspace by atomic
+ * reductions, so dQ's rounding can differ from run to run in the last bits.
+ * With less, the two-kernel form runs (see fa_backward_min_workspace_bytes),
+ * whose results are bitwise reproducible. The environment variable
+ * FA_BWD_ALGO=split selects the two-kernel form whatever the workspace (a
+ * tuning switch).
  */
 fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
                       const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
@@ -227,9 +249,12 @@ fa_status fa_backward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor
  * Arguments, layouts, results and errors are those of fa_backward, minus
  * the workspace. The scratch is a global-memory area of
  * fa_backward_noalloc_max_bytes() bytes (64 MiB) that every device which
- * loads the library reserves until the process exits. A call whose
- * fa_backward_workspace_bytes(B,H,N,d) exceeds it returns FA_ERR_UNSUPPORTED
- * before doing anything, and fa_last_error() states both sizes. The call
+ * loads the library reserves until the process exits. The call runs the
+ * one-pass backward when fa_backward_workspace_bytes(B,H,N,d) fits in the
+ * area, else the two-kernel form; a call whose
+ * fa_backward_min_workspace_bytes(B,H,N,d) exceeds it returns
+ * FA_ERR_UNSUPPORTED before doing anything, and fa_last_error() states both
+ * sizes. The call
  * allocates no memory (no cudaMalloc, no cudaFree, no allocating library
  * routine) as long as the measurement hooks are off, which is the default.
  *
@@ -275,9 +300,9 @@ fa_status fa_debug_configure(unsigned int flags, unsigned long long wait_limit_n
 /*
  * Measurement hooks. Kernels are numbered 0 .. fa_num_kernels()-1:
  * 0 forward, 1 backward preprocess (D_i and LSE*log2 e), 2 backward dK/dV,
- * 3 backward dQ, 4 merge of a split forward, and for head dimension 256 the
- * backward's 5 dV, 6 dK and 7 dQ kernels; fa_kernel_name() names them ("" for
- * an unknown id).
+ * 3 backward dQ, 4 merge of a split forward, for head dimension 256 the
+ * backward's 5 dV, 6 dK and 7 dQ kernels, 8 the one-pass backward and 9 its
+ * dQ conversion; fa_kernel_name() names them ("" for an unknown id).
  *
  * fa_profile_enable(1): from then on every kernel launch is bracketed by two
  * CUDA events recorded on its stream (no synchronisation, no device memory).

@@ -44,15 +44,24 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
+    """Row statistics D and LSE*log2(e) (fp32, padded to whole 128-row query
+    tiles per (batch, head)), then for d <= 128 the one-pass backward's fp32
+    dQ accumulator of d floats per padded row; the minimum is the statistics."""
     B, H, N, d = 4, 16, 4096, 128
     rows = B * H * N
     up = lambda x: (x + 255) // 256 * 256
-    assert lib.fa_backward_workspace_bytes(B, H, N, d) == 2 * up(4 * rows)
-    # statistics are padded to whole 128-row query tiles per (batch, head)
-    assert lib.fa_backward_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * 3 * 5 * 256)
-    assert lib.fa_backward_workspace_bytes(1, 1, 1, 128) == 2 * up(4 * 128)
-    assert lib.fa_backward_workspace_bytes(-1, 1, 128, 64) == 0
-    assert lib.fa_backward_workspace_bytes(1, 1, 0, 64) == 0
+    assert lib.fa_backward_workspace_bytes(B, H, N, d) == 2 * up(4 * rows) + up(4 * rows * d)
+    assert lib.fa_backward_min_workspace_bytes(B, H, N, d) == 2 * up(4 * rows)
+    padded = 3 * 5 * 256
+    assert lib.fa_backward_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * padded) + up(4 * padded * 64)
+    assert lib.fa_backward_min_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * padded)
+    assert lib.fa_backward_workspace_bytes(1, 1, 1, 96) == 2 * up(4 * 128) + up(4 * 128 * 96)
+    # head dimension 256 runs the two-kernel form only: statistics alone
+    assert lib.fa_backward_workspace_bytes(1, 1, 1, 256) == 2 * up(4 * 128)
+    assert lib.fa_backward_min_workspace_bytes(1, 1, 1, 256) == 2 * up(4 * 128)
+    for f in (lib.fa_backward_workspace_bytes, lib.fa_backward_min_workspace_bytes):
+        assert f(-1, 1, 128, 64) == 0
+        assert f(1, 1, 0, 64) == 0
 
 
 A = ctypes.c_void_p(0x10000)     # fake 16-byte aligned addresses: never dereferenced,
@@ -185,8 +194,10 @@ def test_backward_ex_checks_every_operand(lib):
                                 300, 64, 1, 0.125, None, B_, ws_bytes, None)
         assert st == MISALIGNED, k
     r = [ctypes.byref(x) for x in good]
+    # below the row statistics' size (the two-kernel form's minimum)
+    min_bytes = lib.fa_backward_min_workspace_bytes(1, 2, 300, 64)
     assert lib.fa_backward_ex(r[0], r[1], r[2], r[3], r[4], B_, r[5], r[6], r[7], 1, 2, 300, 300,
-                              64, 1, 0.125, None, B_, ws_bytes - 256, None) == INVALID
+                              64, 1, 0.125, None, B_, min_bytes - 256, None) == INVALID
     o32 = desc(dtype=binding.FA_F32)
     assert lib.fa_backward_ex(r[0], r[1], r[2], ctypes.byref(o32), r[4], B_, r[5], r[6], r[7], 1,
                               2, 300, 300, 64, 1, 0.125, None, B_, ws_bytes, None) == UNSUPPORTED

@@ -1,7 +1,8 @@
 """The library inside a CUDA graph. The entry points enqueue work on the
 caller's stream and never allocate or synchronise, so one forward + backward
 can be captured and replayed; replays with new input values (copied into the
-captured buffers) give the eager results bit for bit. The split forward is
+captured buffers) give the eager results bit for bit (dQ of the one-pass
+backward, summed with fp32 atomics, to one bf16 ulp). The split forward is
 captured too (its workspace allocated before the capture)."""
 import pytest
 import torch
@@ -16,15 +17,16 @@ def fa():
     return m
 
 
-@pytest.mark.parametrize("d", [128, 256])
-def test_forward_backward_graph_replays_match_eager(d):
+@pytest.mark.parametrize("d,algo", [(128, "fused"), (128, "split"), (256, "split")])
+def test_forward_backward_graph_replays_match_eager(d, algo):
     B, H, N = 2, 4, 1000
     first = gen.make_inputs(B, H, N, d, case=990)
     q, k, v, do = (first[t].cuda() for t in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty(B, H, N, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(fa().backward_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(fa().backward_workspace_bytes(B, H, N, d, algo), dtype=torch.uint8,
+                     device="cuda")
 
     def step():
         fa().forward(q, k, v, causal=True, out=o, lse=lse)
@@ -48,8 +50,13 @@ def test_forward_backward_graph_replays_match_eager(d):
         step()
         torch.cuda.synchronize()
         assert fa().device_status() == 0
-        for a, b in zip(got, (o, lse, dq, dk, dv)):
+        for a, b in zip(got[:2] + got[3:], (o, lse, dk, dv)):
             assert torch.equal(a, b)
+        if algo == "split":
+            assert torch.equal(got[2], dq)
+        else:  # dQ summed with fp32 atomics: the same up to one bf16 ulp
+            tol = torch.maximum(got[2].float().abs(), dq.float().abs()) * 2.0 ** -7
+            assert ((got[2].float() - dq.float()).abs() <= tol).all()
 
 
 def test_split_forward_in_a_graph():
