@@ -49,6 +49,7 @@ SIGNATURES = {
     "fa_forward_num_splits": ([_i, _i, _i, _i, _i, _i], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward_min_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "fa_backward_one_pass_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_backward": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
     "fa_backward_ex": ([_tp] * 5 + [_vp] + [_tp] * 3 +
                        [_i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp], _i),
@@ -232,14 +233,21 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, block_mas
 
 
 def backward_workspace_bytes(B, H, N, d, algo: str = "auto") -> int:
-    """Workspace bytes of the backward pass for N query rows per (batch, head):
-    enough for the one-pass kernel ("auto", "fused"), or the row statistics
-    only, which selects the two-kernel form ("split")."""
+    """Workspace bytes of the backward pass for N query rows per (batch, head),
+    which select its form: the faster form for the head dimension ("auto"),
+    the one-pass kernel ("fused", d <= 128), or the row statistics only, the
+    two-kernel form ("split")."""
+    lib = _lib_fast()
     if algo == "split":
-        return int(_lib_fast().fa_backward_min_workspace_bytes(B, H, N, d))
-    if algo not in ("auto", "fused"):
+        return int(lib.fa_backward_min_workspace_bytes(B, H, N, d))
+    if algo == "fused":
+        n = int(lib.fa_backward_one_pass_workspace_bytes(B, H, N, d))
+        if n == 0 and B * H * N > 0:
+            raise ValueError(f"the one-pass backward supports d <= 128, not {d}")
+        return n
+    if algo != "auto":
         raise ValueError(f"algo must be 'auto', 'fused' or 'split', not {algo!r}")
-    return int(_lib_fast().fa_backward_workspace_bytes(B, H, N, d))
+    return int(lib.fa_backward_workspace_bytes(B, H, N, d))
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
@@ -249,9 +257,10 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     Shapes and layouts as in ``forward``: q, o, do, dq are [B, H, Nq, d], k, v,
     dk, dv [B, H, Nk, d], all bf16 or all fp16, with any strides over the
     first three dimensions; each gradient takes its input's layout unless
-    given. ``algo`` sizes the workspace when none is given: "auto"/"fused"
-    for the one-pass backward (head dimensions up to 128; dQ accumulated with
-    atomic adds), "split" for the two-kernel form (bitwise reproducible). A
+    given. ``algo`` sizes the workspace when none is given, which selects the
+    form: "auto" (the faster form for the head dimension: one-pass for
+    d <= 96), "fused" (the one-pass backward, d <= 128; dQ accumulated with
+    atomic adds) or "split" (the two-kernel form, bitwise reproducible). A
     given ``workspace`` decides by its size, as fa_backward_ex does.
     """
     B, H, Nq, Nk, d = _shapes(q, (k, v), (o, do))

@@ -16,7 +16,7 @@
 // 128-key K/V tile and loops over the Q tiles that see it (causal: a row of
 // the tile sees one of its keys; block-sparse: mask[i][j]); dK and dV
 // accumulate in tensor memory, and each step's dQ_i partial (dS K_j, fp32) is
-// added into an fp32 accumulator in the workspace with TMA reductions in L2. fa_bwd_pre zeroes that accumulator and fa_bwd_dq_convert scales it and
+// added into an fp32 accumulator in the workspace with reductions in L2. fa_bwd_pre zeroes that accumulator and fa_bwd_dq_convert scales it and
 // rounds it into dQ afterwards.
 //
 // 16 warps:
@@ -26,10 +26,10 @@
 //   warps 4-7   thread = key row: P^T and dS^T over queries 0..63; then dV out
 //   warps 8-11  the same for queries 64..127; then dK out
 //   warps 12-15 dQ reducer, thread = query row: reads dQ_i's partial out of
-//               tensor memory, stages it in shared memory in 32-column chunks
-//               (128-byte swizzle) and adds it into the fp32 accumulator with
-//               TMA tensor reductions (cp.reduce.async.bulk.tensor .add), which
-//               L2 performs a whole line at a time
+//               tensor memory, transposes it through shared memory in 32 x 32
+//               chunks and adds it into the fp32 accumulator with vector
+//               reductions (red.global.add.v4.f32) that each cover four whole
+//               128-byte lines; the TMA unit stays free for the tile loads
 // Registers are moved between the warpgroups with setmaxnreg: the producer /
 // issuer warpgroup and the reducer give some up, the softmax warpgroups take
 // them (88 + 2 x 160 + 104 per thread of each warpgroup: the 65536 the launch
@@ -42,14 +42,14 @@
 // at d = 96 and 128 it reuses the dP^T columns, which are free once the
 // softmax warps have read dP^T(n), and dP^T(n+1) waits until the reducer has
 // read dQ(n) out.
-// Shared memory: K_j, V_j, Q_i ring, dO_i[2], and dS^T (128 keys x 128
-// queries, 16-bit, 128-byte swizzle). dS^T is the A operand of both
-// dK += dS^T Q (read K-major: rows = keys) and dQ_i = dS K_j (read MN-major:
-// M = queries along a row, K = keys down the rows), so dS leaves the softmax
-// warps once, through shared memory. The reducer stages dQ(n) in dO_n's slot
-// (d = 96, 128), which dV(n) and dP^T(n) have finished reading when dQ(n)
-// completes; the slot is released for dO_{n+2} once the reductions have read
-// it. At d = 64 it has a staging area of its own.
+// Shared memory: K_j, V_j, Q_i ring, dO_i[2], the reducer's staging (two 4 KB
+// chunk slots per warp) and dS^T (128 keys x 128 queries, 16-bit, 128-byte
+// swizzle). dS^T is the A operand of both dK += dS^T Q (read K-major: rows =
+// keys) and dQ_i = dS K_j (read MN-major: M = queries along a row, K = keys
+// down the rows), so dS leaves the softmax warps once, through shared memory.
+// At d = 96 and 128 dS^T(n) is written into dO_n's slot once dV(n) has read
+// it (dP^T(n) has already), and the slot takes dO_{n+2} once dK(n) and dQ(n)
+// have read dS^T(n); at d = 64 it has a tile of its own.
 // MMA order per step n: dV(n) (two halves, as P^T(n) arrives), S^T(n+1),
 // dQ(n), dK(n), dP^T(n+1). MMAs issued by one thread execute in issue order,
 // so S^T(n+1) overwrites P^T(n) only after dV(n) has read it.
@@ -74,15 +74,17 @@ struct FusedLayout {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kdOOff = kQOff + kQSlots * kTileBytes;
-  static constexpr int kdSOff = kdOOff + kdOSlots * kTileBytes;    // 128 x 128, two chunks
-  // the reducer's staging: two 4 KB chunk slots per warp, in dO's slot when
-  // that holds 32 KB, else an area of its own
-  static constexpr bool kStageInDo = kTileBytes >= 4 * 2 * 4096;
-  static constexpr int kStageOff = kdSOff + 2 * kChunkBytes;
-  static constexpr int kLseOff = kStageOff + (kStageInDo ? 0 : 4 * 2 * 4096);  // [kQSlots][128]
+  // dS^T (128 x 128, two chunks) of step n goes into dO_n's slot when that
+  // holds 32 KB (d = 96, 128): dV(n) and dP^T(n) have read dO_n by then.
+  // Otherwise it has a tile of its own.
+  static constexpr bool kDsInDo = kTileBytes >= 2 * kChunkBytes;
+  static constexpr int kdSOff = kdOOff + kdOSlots * kTileBytes;
+  // the reducer's staging: two 4 KB chunk slots per warp
+  static constexpr int kStageOff = kdSOff + (kDsInDo ? 0 : 2 * kChunkBytes);
+  static constexpr int kLseOff = kStageOff + 4 * 2 * 4096;          // [kQSlots][128] LSE * log2(e)
   static constexpr int kDeltaOff = kLseOff + kQSlots * kTile * 4;  // [kdOSlots][128] D
   static constexpr int kBarOff = kDeltaOff + kdOSlots * kTile * 4;
-  static constexpr int kNumBars = 23;
+  static constexpr int kNumBars = 24;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -108,6 +110,7 @@ struct Bars {
   __device__ uint32_t dp_full() const { return base + 8 * 14; }
   __device__ uint32_t ds_full() const { return base + 8 * 15; }   // dS^T in shared memory
   __device__ uint32_t ds_empty() const { return base + 8 * 16; }  // dK and dQ have read it
+  __device__ uint32_t dv_step() const { return base + 8 * 23; }   // dV(n) has read dO_n
   __device__ uint32_t dq_full(int b) const { return base + 8 * (17 + b); }
   __device__ uint32_t dq_free(int b) const { return base + 8 * (19 + b); }
   __device__ uint32_t acc_done() const { return base + 8 * 21; }
@@ -127,14 +130,22 @@ __device__ __forceinline__ int next_q(const Shape &sh, int i, int j) {
 // 16kk..16kk+15): queries 64h.. are packed at column 64h.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// Adds the 32 x 32 fp32 box at `src` (shared memory, 128-byte swizzle) into
-// the map's tensor at column x, row y: a TMA tensor reduction performed in L2.
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *tm, uint32_t src, int x,
-                                                  int y) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
-      ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(x), "r"(y)
-      : "memory");
+// Four fp32 values added into global memory at `addr` (16-byte aligned) by
+// one vector reduction performed in L2.
+__device__ __forceinline__ void red_add_v4(float *addr, uint32_t a, uint32_t b, uint32_t c,
+                                           uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr),
+               "f"(__uint_as_float(a)), "f"(__uint_as_float(b)), "f"(__uint_as_float(c)),
+               "f"(__uint_as_float(d))
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
+                                             uint32_t &d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr)
+               : "memory");
 }
 
 template <uint32_t kRegs>
@@ -147,8 +158,8 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 }
 
 // This thread's row of 32 fp32 values into a 4 KB chunk slot (32 rows x 128
-// bytes, 16-byte pieces swizzled by row & 7: the layout of a 32 x 32 box of
-// the dQ accumulator's map).
+// bytes, 16-byte pieces swizzled by row & 7, so that neither this write nor
+// the read-back by rows conflicts on shared-memory banks).
 __device__ __forceinline__ void stage_row32(uint32_t slot, int row, const uint32_t (&v)[32]) {
   const uint32_t base = slot + row * 128;
 #pragma unroll
@@ -197,7 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
     return;
   }
   const uint32_t sK = s_base + L::kKOff, sV = s_base + L::kVOff;
-  const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff, sdS = s_base + L::kdSOff;
+  const uint32_t sQ = s_base + L::kQOff, sdO = s_base + L::kdOOff;
+  // dS^T of step n
+  auto ds_tile = [&](int n) -> uint32_t {
+    return L::kDsInDo ? sdO + (n & 1) * L::kTileBytes : s_base + L::kdSOff;
+  };
   const float *lse_s = reinterpret_cast<const float *>(smem + L::kLseOff);
   const float *delta_s = reinterpret_cast<const float *>(smem + L::kDeltaOff);
   Bars bars{s_base + L::kBarOff};
@@ -227,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
       mbar_init(bars.q_full(s), 1);
       mbar_init(bars.q_empty(s), 1);
     }
-    // a dO slot is free once dV has read dO_i (one commit), the softmax
-    // warps have read D_i (256 threads) and, when the reducer stages dQ in
-    // it, the reducer's 4 warps have had their reductions read it
+    // a dO slot is free once the MMAs are done with it (one commit: after
+    // dV, or after dK and dQ where dS^T goes into the slot) and the softmax
+    // warps have read D_i (256 threads)
     for (int s = 0; s < L::kdOSlots; ++s) {
       mbar_init(bars.do_full(s), 1);
-      mbar_init(bars.do_empty(s), L::kStageInDo ? 261 : 257);
+      mbar_init(bars.do_empty(s), 257);
     }
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.p_full(0), 256);
@@ -240,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.ds_full(), 256);
     mbar_init(bars.ds_empty(), 1);
+    mbar_init(bars.dv_step(), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.dq_full(b), 1);
       mbar_init(bars.dq_free(b), 128);
@@ -340,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         }
       };
       // dK += dS^T Q_i: dS^T K-major (rows = keys), Q_i MN-major (rows = queries)
-      auto issue_dk = [&](uint32_t q_base, bool first_step) {
+      auto issue_dk = [&](uint32_t sdS, uint32_t q_base, bool first_step) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_f16kind_ss(tmem + L::kColDK,
@@ -350,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
       };
       // dQ_i partial = dS K_j: dS read MN-major from the dS^T tile (M =
       // queries along a row), K_j MN-major (N = d along a row); K = keys
-      auto issue_dq = [&](uint32_t col) {
+      auto issue_dq = [&](uint32_t sdS, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_f16kind_ss(tmem + col, sdesc_sw128(sdS + kk * 2048, L::kChunkBytes, 1024),
@@ -384,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         if (!ok) break;
         tc_fence_after();
         issue_dv(sdO + ds * L::kTileBytes, n == 0, 1);
-        mma_commit(bars.do_empty(ds));  // dV(n) has read dO_n
+        if (L::kDsInDo)
+          mma_commit(bars.dv_step());  // dV(n) has read dO_n: dS^T(n) may go there
+        else
+          mma_commit(bars.do_empty(ds));  // dV(n) has read dO_n
         if (inext < T) {
           ok = mbar_wait_inl(bars.q_full(qs1), qph1, st, status_code(kKernBwdFused, kRoleMma, 4));
           if (!ok) break;
@@ -401,11 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
           if (!ok) break;
         }
         tc_fence_after();
-        issue_dq(b ? L::kColDQ1 : L::kColDQ0);
+        issue_dq(ds_tile(n), b ? L::kColDQ1 : L::kColDQ0);
         mma_commit(bars.dq_full(b));
-        issue_dk(sQ + qs * L::kTileBytes, n == 0);
+        issue_dk(ds_tile(n), sQ + qs * L::kTileBytes, n == 0);
         mma_commit(bars.q_empty(qs));
-        mma_commit(bars.ds_empty());
+        if (L::kDsInDo)
+          mma_commit(bars.do_empty(ds));  // dK(n) and dQ(n) have read dS^T(n) in dO_n's slot
+        else
+          mma_commit(bars.ds_empty());
         if (inext < T) {
           if (L::kDqShare) {  // dP^T(n+1) goes where dQ(n) is until it has been read
             ok = mbar_wait_inl(bars.dq_free(0), n & 1, st, status_code(kKernBwdFused, kRoleMma, 10));
@@ -500,14 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
           dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x >> 5][x & 31]) - delta[x]),
                                    pr[x + 1] * (__uint_as_float(dr[x >> 5][(x + 1) & 31]) - delta[x + 1]));
       }
-      // dK(n-1) and dQ(n-1) have read the previous dS^T
-      if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait_inl(bars.ds_empty(), (n - 1) & 1, st,
-                                               status_code(kKernBwdFused, kRoleSoftmax, 7)));
+      // where dS^T(n) goes must be free: dO_n's slot once dV(n) has read it,
+      // or the own tile once dK(n-1) and dQ(n-1) have read it
+      if (L::kDsInDo || n > 0) {
+        ok = __all_sync(0xffffffffu,
+                        L::kDsInDo ? mbar_wait_inl(bars.dv_step(), n & 1, st,
+                                                   status_code(kKernBwdFused, kRoleSoftmax, 9))
+                                   : mbar_wait_inl(bars.ds_empty(), (n - 1) & 1, st,
+                                                   status_code(kKernBwdFused, kRoleSoftmax, 7)));
         if (!ok) break;
       }
       {
-        const uint32_t row = sdS + h * L::kChunkBytes + kr * 128;
+        const uint32_t row = ds_tile(n) + h * L::kChunkBytes + kr * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           st_shared_v4(row + ((uint32_t(u) ^ uint32_t(kr & 7)) << 4), dsp[4 * u], dsp[4 * u + 1],
@@ -536,27 +562,35 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
     const int lane = threadIdx.x & 31;
     const uint32_t t = tmem + (uint32_t(qw * 32) << 16);
     constexpr int kParts = D / 32;                  // 32-column chunks of a dQ row: 2, 3, 4
-    const int row0 = (int)stat_head + 32 * qw;      // the warp's first row in the accumulator
+    float *dq_head = p.dq_acc + stat_head * D;      // this head's [tq*128][D] accumulator
+    const uint32_t slot = s_base + L::kStageOff + qw * 8192;  // this warp's two 4 KB slots
+    // Adds a staged 32 x 32 chunk (columns col0..col0+31 of the warp's rows)
+    // into the accumulator: lane l reads 16 bytes of row 4k + l/8, so each
+    // reduction instruction covers 4 rows x 128 bytes, whole L2 lines.
+    auto flush = [&](uint32_t sl, int i, int col0) {
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + (lane >> 3), pc = lane & 7;
+        uint32_t a, b, c, d;
+        ld_shared_v4(sl + r * 128 + ((uint32_t(pc) ^ uint32_t(r & 7)) << 4), a, b, c, d);
+        const int row = kTile * i + 32 * qw + r;
+        if (row < sh.nq) red_add_v4(dq_head + (size_t)row * D + col0 + 4 * pc, a, b, c, d);
+      }
+      __syncwarp();  // the slot may be written again
+    };
     bool ok = true;
     int n = 0;
     for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
       const int b = L::kDqShare ? 0 : (n & 1);
       ok = __all_sync(0xffffffffu,
                       mbar_wait_inl(bars.dq_full(b), L::kDqShare ? (n & 1) : ((n >> 1) & 1), st,
-                                status_code(kKernBwdFused, kRoleSoftmax, 8)));
+                                    status_code(kKernBwdFused, kRoleSoftmax, 8)));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tq = t + (b ? L::kColDQ1 : L::kColDQ0);
-      // this warp's two 4 KB chunk slots: in dO_n's slot (read by dV(n) and
-      // dP^T(n), both complete with dQ(n)) or in the staging area, whose
-      // previous reductions must have read it first
-      const uint32_t slot = (L::kStageInDo ? sdO + (n & 1) * L::kTileBytes
-                                           : s_base + L::kStageOff) + qw * 8192;
-      if (!L::kStageInDo && n > 0) {
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
-      }
-      const int y = row0 + kTile * i;
+      // columns 0..63 into the two slots; the rest into registers before the
+      // tensor-memory columns are released, so that dQ's buffer frees early
       {
         uint32_t v[2][32];
         tmem_ld32(tq, v[0]);
@@ -569,13 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         stage_row32(slot, lane, v[0]);
         stage_row32(slot + 4096, lane, v[1]);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_2d(&p.tm_dqacc, slot, 0, y);
-        tma_reduce_add_2d(&p.tm_dqacc, slot + 4096, 32, y);
-        bulk_commit_group();
-      }
       if (kParts > 2) {
         uint32_t v[2][32];
         tmem_ld32(tq + 64, v[0]);
@@ -583,29 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bars.dq_free(b));
-        if (lane == 0) bulk_wait_group_read0();  // chunks 0 and 1 have left the slots
-        __syncwarp();
+        flush(slot, i, 0);
         stage_row32(slot, lane, v[0]);
+        flush(slot + 4096, i, 32);
         if (kParts > 3) stage_row32(slot + 4096, lane, v[1]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&p.tm_dqacc, slot, 64, y);
-          if (kParts > 3) tma_reduce_add_2d(&p.tm_dqacc, slot + 4096, 96, y);
-          bulk_commit_group();
-        }
-      }
-      if (L::kStageInDo) {  // dO_n's slot may take dO_{n+2} once the reductions have read it
-        if (lane == 0) {
-          bulk_wait_group_read0();
-          mbar_arrive(bars.do_empty(n & 1));
-        }
-        __syncwarp();
+        flush(slot, i, 64);
+        if (kParts > 3) flush(slot + 4096, i, 96);
+      } else {
+        flush(slot, i, 0);
+        flush(slot + 4096, i, 32);
       }
     }
-    // the CTA's shared memory must outlive the reductions' reads of it
-    if (lane == 0) bulk_wait_group_read0();
-    __syncwarp();
   }
 
   tc_fence_before();

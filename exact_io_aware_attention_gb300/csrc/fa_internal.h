@@ -105,8 +105,6 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
   CUtensorMap tm_dq, tm_dk, tm_dv;     // maps over the gradients, 64 x 32 boxes (TMA stores)
-  CUtensorMap tm_dqacc;                // one-pass backward: 2-D map over dq_acc ([rows][d] fp32),
-                                       // 32 x 32 boxes, 128-byte swizzle (TMA reductions)
   Shape sh;
   const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;

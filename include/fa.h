@@ -181,24 +181,32 @@ size_t fa_forward_split_workspace_bytes(int B, int H, int Nq, int d, int num_spl
 int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal);
 
 /*
- * Bytes of device workspace with which fa_backward and fa_backward_ex run the
- * one-pass backward, for N query rows per (batch, head): fp32 D
- * (D_i = dO_i.O_i) and fp32 LSE*log2(e), each [B,H,ceil(N/128)*128], then
- * (d <= 128) an fp32 dQ accumulator [B,H,ceil(N/128)*128,d], each part
- * starting on a 256-byte boundary: O(N*d), 8 + 4d bytes per query row.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_backward and fa_backward_ex need for N query
+ * rows per (batch, head) in their default form for head dimension d: fp32 D
+ * (D_i = dO_i.O_i) and fp32 LSE*log2(e), each [B,H,ceil(N/128)*128], and for
+ * d <= 96 (where the one-pass backward is the default) an fp32 dQ accumulator
+ * [B,H,ceil(N/128)*128,d], each part on a 256-byte boundary: O(N*d), 8 + 4d
+ * bytes per query row for d <= 96, 8 otherwise. Returns 0 for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * The smallest workspace fa_backward and fa_backward_ex accept: the two
- * statistics only, 8 bytes per query row (O(N)). With less than
- * fa_backward_workspace_bytes (or with d = 256) the backward runs the
- * two-kernel form, which recomputes S and dP in a second kernel that owns dQ
- * instead of accumulating dQ in the workspace: slower, same results up to
- * rounding order. Returns 0 for invalid sizes.
+ * statistics only, 8 bytes per query row (O(N)). It selects the two-kernel
+ * backward, which recomputes S and dP in a second kernel that owns dQ instead
+ * of accumulating dQ in the workspace. Returns 0 for invalid sizes.
  */
 size_t fa_backward_min_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * The workspace that selects the one-pass backward (d <= 128): the statistics
+ * and the fp32 dQ accumulator, 8 + 4d bytes per query row. Equal to
+ * fa_backward_workspace_bytes for d <= 96; at d = 128 it opts into the
+ * one-pass form, which there ties with the two-kernel default (causal) or
+ * trails it by a few percent (non-causal). Returns 0 for d = 256 (two-kernel
+ * form only) and for invalid sizes.
+ */
+size_t fa_backward_one_pass_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * Backward pass. Reads Q, K, V, O, dO (bf16) and LSE (fp32, as written by the
@@ -208,13 +216,15 @@ size_t fa_backward_min_workspace_bytes(int B, int H, int N, int d);
  * contents on entry do not matter and are clobbered. The score and
  * probability tiles are recomputed on chip and never reach global memory.
  *
- * With at least fa_backward_workspace_bytes(B,H,N,d) bytes (d <= 128) one
- * kernel recomputes S and P once per (Q tile, K/V tile) pair and runs all
- * five products there: dK and dV accumulate on chip, and each pair's dQ
- * partial is added into the fp32 accumulator in the workspace by atomic
- * reductions, so dQ's rounding can differ from run to run in the last bits.
- * With less, the two-kernel form runs (see fa_backward_min_workspace_bytes),
- * whose results are bitwise reproducible. The environment variable
+ * The workspace size selects the form. With at least
+ * fa_backward_one_pass_workspace_bytes(B,H,N,d) bytes (d <= 128) one kernel
+ * recomputes S and P once per (Q tile, K/V tile) pair and runs all five
+ * products there: dK and dV accumulate on chip, and each pair's dQ partial
+ * is added into the fp32 accumulator in the workspace by atomic reductions,
+ * so dQ's rounding can differ from run to run in the last bits. With less
+ * (at least fa_backward_min_workspace_bytes), the two-kernel form runs, whose
+ * results are bitwise reproducible. fa_backward_workspace_bytes gives the
+ * faster form's size for each head dimension. The environment variable
  * FA_BWD_ALGO=split selects the two-kernel form whatever the workspace (a
  * tuning switch).
  */
@@ -250,8 +260,8 @@ fa_status fa_backward_ex(const fa_tensor *Q, const fa_tensor *K, const fa_tensor
  * the workspace. The scratch is a global-memory area of
  * fa_backward_noalloc_max_bytes() bytes (64 MiB) that every device which
  * loads the library reserves until the process exits. The call runs the
- * one-pass backward when fa_backward_workspace_bytes(B,H,N,d) fits in the
- * area, else the two-kernel form; a call whose
+ * default form when fa_backward_workspace_bytes(B,H,N,d) fits in the area,
+ * else the two-kernel form; a call whose
  * fa_backward_min_workspace_bytes(B,H,N,d) exceeds it returns
  * FA_ERR_UNSUPPORTED before doing anything, and fa_last_error() states both
  * sizes. The call

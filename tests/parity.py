@@ -70,3 +70,22 @@ def check_grad(g, g_ref, name, what=""):
     r = rel_l2(g, g_ref)
     assert r <= GRAD_REL_L2, f"{what} {name} rel_l2={r:.3e}"
     return r
+
+
+def assert_same_up_to_atomics(x, y, what=""):
+    """Two bf16 results of the one-pass backward's dQ, whose fp32 partial sums
+    are added with atomics in whatever order the CTAs reach L2: equal up to one
+    bf16 ulp of the larger value, plus an absolute floor of 1e-5 of the
+    tensor's largest magnitude for elements that cancel to near zero (where
+    the fp32 summation order alone moves the value by more than its ulp). A
+    real defect (a lost or doubled partial) moves elements by O(1) relative."""
+    xf, yf = x.float(), y.float()
+    floor = 1e-5 * float(yf.abs().max())
+    tol = torch.maximum(xf.abs(), yf.abs()) * 2.0 ** -7 + floor
+    err = (xf - yf).abs()
+    bad = err > tol
+    if bad.any():
+        k = int(torch.argmax(err - tol))
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.numel()} elements differ beyond one ulp; worst "
+            f"{float(xf.flatten()[k]):.6e} vs {float(yf.flatten()[k]):.6e}")

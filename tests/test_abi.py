@@ -45,21 +45,27 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     """Row statistics D and LSE*log2(e) (fp32, padded to whole 128-row query
-    tiles per (batch, head)), then for d <= 128 the one-pass backward's fp32
-    dQ accumulator of d floats per padded row; the minimum is the statistics."""
-    B, H, N, d = 4, 16, 4096, 128
-    rows = B * H * N
+    tiles per (batch, head)); the one-pass backward adds an fp32 dQ accumulator
+    of d floats per padded row. The default size is the faster form's: the
+    one-pass form for d <= 96, the two-kernel form (statistics only) above."""
     up = lambda x: (x + 255) // 256 * 256
-    assert lib.fa_backward_workspace_bytes(B, H, N, d) == 2 * up(4 * rows) + up(4 * rows * d)
-    assert lib.fa_backward_min_workspace_bytes(B, H, N, d) == 2 * up(4 * rows)
+    B, H, N = 4, 16, 4096
+    rows = B * H * N
+    stats = 2 * up(4 * rows)
+    for d in (64, 96):
+        assert lib.fa_backward_workspace_bytes(B, H, N, d) == stats + up(4 * rows * d)
+        assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, d) == stats + up(4 * rows * d)
+    assert lib.fa_backward_workspace_bytes(B, H, N, 128) == stats
+    assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, 128) == stats + up(4 * rows * 128)
+    assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, 256) == 0
+    for d in (64, 96, 128, 256):
+        assert lib.fa_backward_min_workspace_bytes(B, H, N, d) == stats
     padded = 3 * 5 * 256
     assert lib.fa_backward_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * padded) + up(4 * padded * 64)
     assert lib.fa_backward_min_workspace_bytes(3, 5, 129, 64) == 2 * up(4 * padded)
-    assert lib.fa_backward_workspace_bytes(1, 1, 1, 96) == 2 * up(4 * 128) + up(4 * 128 * 96)
-    # head dimension 256 runs the two-kernel form only: statistics alone
     assert lib.fa_backward_workspace_bytes(1, 1, 1, 256) == 2 * up(4 * 128)
-    assert lib.fa_backward_min_workspace_bytes(1, 1, 1, 256) == 2 * up(4 * 128)
-    for f in (lib.fa_backward_workspace_bytes, lib.fa_backward_min_workspace_bytes):
+    for f in (lib.fa_backward_workspace_bytes, lib.fa_backward_min_workspace_bytes,
+              lib.fa_backward_one_pass_workspace_bytes):
         assert f(-1, 1, 128, 64) == 0
         assert f(1, 1, 0, 64) == 0
 

@@ -13,7 +13,8 @@ from exact_io_aware_attention_gb300 import binding
 from exact_io_aware_attention_gb300 import inputs as gen
 from parity import check_grad, check_lse, check_o_bf16, f64
 
-KERNELS = {1: "forward", 3: "dK/dV", 4: "dQ", 5: "dV (d=256)", 6: "dK (d=256)", 7: "dQ (d=256)"}
+KERNELS = {1: "forward", 3: "dK/dV", 4: "dQ", 5: "dV (d=256)", 6: "dK (d=256)", 7: "dQ (d=256)",
+           8: "one-pass backward"}
 ROLES = {1: "load", 2: "mma", 3: "softmax", 4: "dq"}
 
 
@@ -41,9 +42,12 @@ def test_stalled_producer_is_reported_and_the_context_survives(d):
         assert kern == 1 and role in (2, 3), (kern, role, site)
         o0 = torch.zeros_like(q)
         lse0 = torch.zeros(q.shape[:3], device="cuda")
-        binding.backward(q, k, v, o0, do, lse0, causal=True)
-        kern, role, site = decode(binding.device_status())
-        assert kern in ((3, 4) if d < 256 else (5, 6, 7)) and role in (2, 3), (kern, role, site)
+        # both backward forms where the head dimension has both
+        for algo, kernels in ((("fused", (8,)), ("split", (3, 4))) if d < 256
+                              else (("split", (5, 6, 7)),)):
+            binding.backward(q, k, v, o0, do, lse0, causal=True, algo=algo)
+            kern, role, site = decode(binding.device_status())
+            assert kern in kernels and role in (2, 3), (algo, kern, role, site)
     finally:
         lib.fa_debug_configure(0, 0)
     # the context is intact: a normal forward and backward are correct

@@ -63,7 +63,7 @@ def test_random_configuration(seed):
     o, lse = fa().forward(q, k, v, causal=c["causal"], block_mask=m, num_splits=c["splits"])
     torch.cuda.synchronize()
     assert fa().device_status() == 0
-    what = f"seed={seed} {c} backward={'split' if seed % 4 == 0 else 'auto'}"
+    what = f"seed={seed} {c} backward={'split' if seed % 4 == 0 or d > 128 else 'fused'}"
     check_o(f64(o32), o_ref, what)
     check_lse(f64(lse32), lse_ref, what)
     check_lse(f64(lse), lse_ref, what)
@@ -73,8 +73,8 @@ def test_random_configuration(seed):
     assert np.sqrt(max(0.0, r * r - r_floor * r_floor)) <= 2e-3, what
     g = oracle.backward(*x, causal=c["causal"], scale=scale, block_mask=mk)
     # every fourth case runs the two-kernel backward form, the others the
-    # one-pass form (the default where the head dimension allows it)
-    algo = "split" if seed % 4 == 0 else "auto"
+    # one-pass form where the head dimension has it (d <= 128)
+    algo = "split" if seed % 4 == 0 or d > 128 else "fused"
     dq, dk, dv = fa().backward(q, k, v, o, do, lse, causal=c["causal"], block_mask=m, algo=algo)
     torch.cuda.synchronize()
     assert fa().device_status() == 0
