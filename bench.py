@@ -192,7 +192,8 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
     "fa_bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
     "fa_bwd_dq": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
-    "fa_bwd_fused": ("fa_bwd_fused.cu", "ptx.cuh", "fa_internal.h", "tile_store.cuh"),
+    "fa_bwd_fused": ("fa_bwd_fused.cu", "fa_bwd_fused_q64.cu", "ptx.cuh", "fa_internal.h",
+                     "tile_store.cuh"),
 }
 
 

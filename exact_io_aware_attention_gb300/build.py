@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_bwd_d256.cu",
-           "fa_bwd_fused.cu"]
+           "fa_bwd_fused.cu", "fa_bwd_fused_q64.cu"]
 HEADERS = ["ptx.cuh", "fa_internal.h", "tile_store.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -143,6 +143,29 @@ bool encode_operand(CUtensorMap *m, const void *base, const fa::RowStrides &st, 
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the one-pass backward's fp32 dQ accumulator: `rows` rows of d
+// floats, 32 x 32 boxes (128 bytes wide) in the 128-byte swizzle, for the
+// kernels' TMA tensor reductions.
+bool encode_dq_acc(CUtensorMap *m, float *base, long long rows, int d) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    snprintf(g_last_error, sizeof(g_last_error),
+             "cuTensorMapEncodeTiled(dQ accumulator %p, rows=%lld, d=%d) failed: CUresult %d",
+             (void *)base, rows, d, (int)r);
+  return r == CUDA_SUCCESS;
+}
+
 // Heads per CTA group of the backward grid (kept small so the fp32 dQ rows
 // that concurrent CTAs accumulate stay in L2). FA_BWD_HEAD_GROUP overrides it
 // for tuning runs.
@@ -342,16 +365,19 @@ size_t dq_acc_bytes(int B, int H, int Nq, int d) {
 }
 
 // The default form by head dimension, from interleaved A/B timings of both
-// forms on GB300: the one-pass kernel is 18-25 % faster at d = 64 and 3-4 %
-// at d = 96; at d = 128 its dQ partial must share tensor memory with dP^T and
-// it ties with the two-kernel form (causal) or trails it by 3-5 % (dense).
-bool one_pass_by_default(int d) { return d <= 96; }
+// forms on GB300: the one-pass kernels are 18-25 % faster at d = 64, 3-4 % at
+// d = 96 and 1-7.5 % at d = 128 (64-query steps); d = 256 has the two-kernel
+// form only.
+bool one_pass_by_default(int d) { return d <= 128; }
 
 // Whether a backward with this much workspace runs the one-pass kernel: the
 // workspace holds the dQ accumulator too, and FA_BWD_ALGO=split (a tuning and
 // A/B switch) does not ask for the two-kernel form.
 bool use_one_pass(int B, int H, int Nq, int d, size_t ws_bytes) {
   if (d > 128) return false;
+  // the accumulator's rows are addressed with 32-bit TMA coordinates
+  if ((long long)B * H * ((Nq + fa::kTile - 1) / fa::kTile) * fa::kTile > 0x7fffffffLL)
+    return false;
   const char *e = getenv("FA_BWD_ALGO");
   if (e && strcmp(e, "split") == 0) return false;
   return ws_bytes >= stats_workspace_bytes(B, H, Nq) + dq_acc_bytes(B, H, Nq, d);
@@ -409,6 +435,9 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   p.dq_acc = use_one_pass(B, H, Nq, d, ws_bytes)
                  ? reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * stat_bytes)
                  : nullptr;
+  if (p.dq_acc && d == 128 &&
+      !encode_dq_acc(&p.tm_dqacc, p.dq_acc, (long long)B * H * p.sh.tq * fa::kTile, d))
+    return FA_ERR_CUDA;
   p.dq = dQ->data;
   p.dk = dK->data;
   p.dv = dV->data;

@@ -12,7 +12,11 @@
 //   dQ_i = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i.
 //
 // Here each (Q tile, K/V tile) pair has S and P recomputed once, and all five
-// products of the pair run on the tensor cores of one CTA. The CTA owns a
+// products of the pair run on the tensor cores of one CTA. This file's kernel
+// serves head dimensions 64 and 96 (128-query steps); head dimension 128 has a
+// kernel of its own with 64-query steps (fa_bwd_fused_q64.cu), because at 128
+// the five products of a 128-query step do not fit in tensor memory side by
+// side. The CTA owns a
 // 128-key K/V tile and loops over the Q tiles that see it (causal: a row of
 // the tile sees one of its keys; block-sparse: mask[i][j]); dK and dV
 // accumulate in tensor memory, and each step's dQ_i partial (dS K_j, fp32) is
@@ -655,29 +659,39 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
   *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.dq) + p.sdq.row(b_idx, h_idx, n) + 8 * g) = o;
 }
 
+// dQ = bf16(scale * dQ_acc) after the one-pass kernel
 template <int D, bool kF16>
-cudaError_t launch_fused_d(const BwdParams &p, cudaStream_t stream) {
-  using L = FusedLayout<D>;
-  static bool configured = false;
-  cudaError_t e;
-  if (!configured) {
-    e = cudaFuncSetAttribute(fa_bwd_fused<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  {
-    LaunchProbe probe(kKindBwdFused, stream);
-    fa_bwd_fused<D, kF16><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+cudaError_t launch_dq_convert(const BwdParams &p, cudaStream_t stream) {
   {
     LaunchProbe probe(kKindBwdConvert, stream);
     const long long total = (long long)p.sh.bh * p.sh.nq * (D / 8);
     fa_bwd_dq_convert<D, kF16><<<unsigned((total + 255) / 256), 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
+}
+
+template <int D, bool kF16>
+cudaError_t launch_fused_d(const BwdParams &p, cudaStream_t stream) {
+  cudaError_t e;
+  if constexpr (D == 128) {
+    e = launch_backward_fused_q64(p, stream);  // 64-query steps (fa_bwd_fused_q64.cu)
+  } else {
+    using L = FusedLayout<D>;
+    static bool configured = false;
+    if (!configured) {
+      e = cudaFuncSetAttribute(fa_bwd_fused<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               L::kBytes);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    {
+      LaunchProbe probe(kKindBwdFused, stream);
+      fa_bwd_fused<D, kF16><<<p.sh.tk * p.sh.bh, kThreads, L::kBytes, stream>>>(p);
+    }
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
+  return launch_dq_convert<D, kF16>(p, stream);
 }
 
 }  // namespace

@@ -105,6 +105,8 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do; // as in FwdParams
   CUtensorMap tm_dq, tm_dk, tm_dv;     // maps over the gradients, 64 x 32 boxes (TMA stores)
+  CUtensorMap tm_dqacc;                // one-pass backward at d = 128: 2-D map over dq_acc
+                                       // ([rows][128] fp32), 32 x 32 boxes, 128-byte swizzle
   Shape sh;
   const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;
@@ -150,6 +152,8 @@ cudaError_t launch_backward_dq(const BwdParams &p, cudaStream_t stream);  // fa_
 // dK, dV and the dQ partials in one kernel, then the dQ conversion, after
 // fa_bwd_pre has zeroed p.dq_acc; head dimensions 64, 96, 128 (fa_bwd_fused.cu)
 cudaError_t launch_backward_fused(const BwdParams &p, cudaStream_t stream);
+// The one-pass kernel for head dimension 128 in 64-query steps (fa_bwd_fused_q64.cu)
+cudaError_t launch_backward_fused_q64(const BwdParams &p, cudaStream_t stream);
 // dV, dK and dQ for head dimension 256, after fa_bwd_pre (fa_bwd_d256.cu)
 cudaError_t launch_backward_d256(const BwdParams &p, cudaStream_t stream);
 

@@ -184,9 +184,10 @@ int fa_forward_num_splits(int B, int H, int Nq, int Nk, int d, int causal);
  * Bytes of device workspace fa_backward and fa_backward_ex need for N query
  * rows per (batch, head) in their default form for head dimension d: fp32 D
  * (D_i = dO_i.O_i) and fp32 LSE*log2(e), each [B,H,ceil(N/128)*128], and for
- * d <= 96 (where the one-pass backward is the default) an fp32 dQ accumulator
- * [B,H,ceil(N/128)*128,d], each part on a 256-byte boundary: O(N*d), 8 + 4d
- * bytes per query row for d <= 96, 8 otherwise. Returns 0 for invalid sizes.
+ * d <= 128 (where the one-pass backward is the default) an fp32 dQ
+ * accumulator [B,H,ceil(N/128)*128,d], each part on a 256-byte boundary:
+ * O(N*d), 8 + 4d bytes per query row for d <= 128, 8 for d = 256. Returns 0
+ * for invalid sizes.
  */
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
@@ -194,16 +195,16 @@ size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
  * The smallest workspace fa_backward and fa_backward_ex accept: the two
  * statistics only, 8 bytes per query row (O(N)). It selects the two-kernel
  * backward, which recomputes S and dP in a second kernel that owns dQ instead
- * of accumulating dQ in the workspace. Returns 0 for invalid sizes.
+ * of accumulating dQ in the workspace: a few percent (d = 128) to 25 % (d = 64)
+ * slower, bitwise reproducible, and with 4d fewer bytes of workspace per row.
+ * Returns 0 for invalid sizes.
  */
 size_t fa_backward_min_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * The workspace that selects the one-pass backward (d <= 128): the statistics
- * and the fp32 dQ accumulator, 8 + 4d bytes per query row. Equal to
- * fa_backward_workspace_bytes for d <= 96; at d = 128 it opts into the
- * one-pass form, which there ties with the two-kernel default (causal) or
- * trails it by a few percent (non-causal). Returns 0 for d = 256 (two-kernel
+ * and the fp32 dQ accumulator, 8 + 4d bytes per query row; equal to
+ * fa_backward_workspace_bytes for d <= 128. Returns 0 for d = 256 (two-kernel
  * form only) and for invalid sizes.
  */
 size_t fa_backward_one_pass_workspace_bytes(int B, int H, int N, int d);

@@ -45,14 +45,14 @@ static float from_bf16(uint16_t h) {
 int main(int argc, char **argv) {
   CHECK(fa_abi_version() == 2);
   CHECK(strcmp(fa_status_string(FA_ERR_MISALIGNED), "FA_ERR_MISALIGNED") == 0);
-  /* row statistics (2 x fp32 per padded row) + the one-pass form's fp32 dQ accumulator,
-     the default form at d = 64; statistics only at d = 128 (two-kernel default) */
+  /* row statistics (2 x fp32 per padded row) + the one-pass form's fp32 dQ accumulator
+     (the default form for d <= 128); statistics only at d = 256 (two-kernel form) */
   CHECK(fa_backward_workspace_bytes(2, 3, 200, 64) ==
         2 * (size_t)(2 * 3 * 256 * 4) + (size_t)(2 * 3 * 256 * 64 * 4));
   CHECK(fa_backward_min_workspace_bytes(2, 3, 200, 64) == 2 * (size_t)(2 * 3 * 256 * 4));
-  CHECK(fa_backward_workspace_bytes(2, 3, 200, 128) == 2 * (size_t)(2 * 3 * 256 * 4));
   CHECK(fa_backward_one_pass_workspace_bytes(2, 3, 200, 128) ==
         2 * (size_t)(2 * 3 * 256 * 4) + (size_t)(2 * 3 * 256 * 128 * 4));
+  CHECK(fa_backward_workspace_bytes(2, 3, 200, 256) == 2 * (size_t)(2 * 3 * 256 * 4));
   CHECK(fa_forward(NULL, NULL, NULL, NULL, NULL, 1, 1, 0, 64, 0, 0.125f, NULL, NULL) == FA_OK);
   CHECK(fa_forward((void *)16, (void *)16, (void *)16, (void *)16, (float *)16, 1, 1, 128, 80,
                    0, 0.125f, NULL, NULL) == FA_ERR_UNSUPPORTED);

@@ -47,16 +47,15 @@ def test_workspace_bytes(lib):
     """Row statistics D and LSE*log2(e) (fp32, padded to whole 128-row query
     tiles per (batch, head)); the one-pass backward adds an fp32 dQ accumulator
     of d floats per padded row. The default size is the faster form's: the
-    one-pass form for d <= 96, the two-kernel form (statistics only) above."""
+    one-pass form for d <= 128, the two-kernel form (statistics only) at 256."""
     up = lambda x: (x + 255) // 256 * 256
     B, H, N = 4, 16, 4096
     rows = B * H * N
     stats = 2 * up(4 * rows)
-    for d in (64, 96):
+    for d in (64, 96, 128):
         assert lib.fa_backward_workspace_bytes(B, H, N, d) == stats + up(4 * rows * d)
         assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, d) == stats + up(4 * rows * d)
-    assert lib.fa_backward_workspace_bytes(B, H, N, 128) == stats
-    assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, 128) == stats + up(4 * rows * 128)
+    assert lib.fa_backward_workspace_bytes(B, H, N, 256) == stats
     assert lib.fa_backward_one_pass_workspace_bytes(B, H, N, 256) == 0
     for d in (64, 96, 128, 256):
         assert lib.fa_backward_min_workspace_bytes(B, H, N, d) == stats

@@ -14,8 +14,13 @@ checks that
     (cudaMemGetInfo) and the caching allocator's peak are unchanged across
     the two calls;
   - the extra memory beyond the inputs and outputs is exactly the LSE plus
-    fa_backward_workspace_bytes, which is O(N) (it is printed beside the
-    bytes a 16-bit score matrix would need).
+    fa_backward_workspace_bytes, which is linear in N (it is printed beside
+    the bytes a 16-bit score matrix would need).
+
+The default (one-pass) backward's workspace holds an fp32 dQ accumulator,
+4d bytes per query row; a second backward with fa_backward_min_workspace_bytes
+(the two-kernel form, 8 bytes per row) shows the smallest footprint, again
+without any allocation.
 """
 import ctypes
 
@@ -75,6 +80,19 @@ def test_long_context_extra_memory_is_lse_plus_workspace():
 
     assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
     assert peak == allocated0, f"the caching allocator grew by {peak - allocated0} bytes"
+    # the two-kernel form with the smallest workspace (a prefix of the same buffer)
+    min_bytes = lib.fa_backward_min_workspace_bytes(B, H, N, d)
+    dq2 = torch.empty_like(q)
+    torch.cuda.synchronize()
+    free2 = torch.cuda.mem_get_info()[0]
+    rc = lib.fa_backward(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq2), _p(dk), _p(dv),
+                         B, H, N, d, 1, w.scale, None, _p(ws), min_bytes, stream)
+    assert rc == 0, lib.fa_last_error().decode()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free2
+    assert binding.device_status() == 0
+    rel = float((dq2.float() - dq.float()).norm() / dq.float().norm())
+    assert rel < 1e-3, f"the two backward forms disagree on dQ: rel-L2 {rel:.2e}"
     # O(N) extra memory: 4 bytes of LSE plus the workspace's bytes per query
     # row, against 2 N bytes per row for a 16-bit score matrix
     rows = B * H * N
@@ -84,7 +102,9 @@ def test_long_context_extra_memory_is_lse_plus_workspace():
     assert per_row <= 4 + 8 + 4 * d + 1, f"{per_row:.1f} extra bytes per query row"
     print(f"\nlong-context extra memory: inputs+outputs {io_bytes / 1e9:.3f} GB; "
           f"LSE {lse.numel() * 4 / 1e6:.1f} MB + workspace {ws_bytes / 1e6:.1f} MB = "
-          f"{extra_bytes / 1e6:.1f} MB ({per_row:.1f} B per query row); "
+          f"{extra_bytes / 1e6:.1f} MB ({per_row:.1f} B per query row); with the smallest "
+          f"workspace (two-kernel form) {(lse.numel() * 4 + min_bytes) / 1e6:.1f} MB "
+          f"({(lse.numel() * 4 + min_bytes) / rows:.1f} B per row); "
           f"a 16-bit score matrix would be {s_bytes / 1e9:.1f} GB; "
           f"cudaMemGetInfo free before/after {free0}/{free1}")
 

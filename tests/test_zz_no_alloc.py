@@ -8,9 +8,8 @@ The GPU test calls it through the C ABI, twice in a row on different shapes
 (the second call reuses the area the first one left behind). The kernels see
 the same inputs as fa_backward with a caller-allocated workspace, so dK and dV
 must equal that call's bit for bit, and so must dQ where the two-kernel form
-runs (the default for head dimensions 128 and 256); the one-pass form (the
-default for 64) sums dQ with fp32 atomics, so there dQ must agree to one bf16
-ulp. The first call is also held to the fp64
+runs (head dimension 256); the one-pass form (the default for 64 to 128) sums
+dQ with fp32 atomics, so there dQ must agree to one bf16 ulp. The first call is also held to the fp64
 oracle. The device's free memory is read before and after
 each call: a call that allocated would change it. This file is collected last
 so that a run stopping at its first failure has already run every other
@@ -76,7 +75,7 @@ def test_noalloc_backward_matches_workspace_backward(lib):
             f"call {n + 1}: free device memory went from {free_before} to {free_after} bytes"
         for name, got, want in (("dk", dk, ref[1]), ("dv", dv, ref[2])):
             assert torch.equal(got, want), f"call {n + 1}: {name} differs from fa_backward"
-        if d > 96:  # the two-kernel form (the default there): bit for bit
+        if d > 128:  # the two-kernel form (the only form there): bit for bit
             assert torch.equal(dq, ref[0]), f"call {n + 1}: dq differs from fa_backward"
         else:  # the one-pass backward sums dQ with fp32 atomics: one bf16 ulp
             assert_same_up_to_atomics(dq, ref[0], f"call {n + 1}: dq against fa_backward")
