@@ -436,7 +436,9 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
                  ? reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * stat_bytes)
                  : nullptr;
   if (p.dq_acc && d == 128 &&
-      !encode_dq_acc(&p.tm_dqacc, p.dq_acc, (long long)B * H * p.sh.tq * fa::kTile, d))
+      (!encode_dq_acc(&p.tm_dqacc, p.dq_acc, (long long)B * H * p.sh.tq * fa::kTile, d) ||
+       !encode_operand(&p.tm_qh, Q->data, sq, B, H, Nq, d, f16, 64) ||
+       !encode_operand(&p.tm_doh, dO->data, p.sdo, B, H, Nq, d, f16, 64)))
     return FA_ERR_CUDA;
   p.dq = dQ->data;
   p.dk = dK->data;

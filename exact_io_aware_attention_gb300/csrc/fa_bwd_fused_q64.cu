@@ -54,18 +54,21 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kD = 128;
 constexpr int kChunkBytes = kTile * 128;     // 128 rows x 128 bytes
-constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit tile
-constexpr int kQSlots = 2, kdOSlots = 2;
+constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit tile (K_j, V_j)
+constexpr int kStep = 64;                    // queries per step
+constexpr int kHalfChunk = kStep * 128;      // 64 rows x 128 bytes
+constexpr int kHalfBytes = 2 * kHalfChunk;   // 64 rows of Q or dO (16 KB)
+constexpr int kQSlots = 4, kdOSlots = 3, kdSBufs = 2;
 constexpr int kKOff = 0;
 constexpr int kVOff = kKOff + kTileBytes;
-constexpr int kQOff = kVOff + kTileBytes;
-constexpr int kdOOff = kQOff + kQSlots * kTileBytes;
-constexpr int kdSOff = kdOOff + kdOSlots * kTileBytes;  // dS^T: 128 keys x 64 queries
-constexpr int kStageOff = kdSOff + kTile * 128;         // the reducer's 4 KB per warp
-constexpr int kLseOff = kStageOff + 4 * 4096;           // [kQSlots][128] LSE * log2(e)
-constexpr int kDeltaOff = kLseOff + kQSlots * kTile * 4;  // [kdOSlots][128] D
-constexpr int kBarOff = kDeltaOff + kdOSlots * kTile * 4;
-constexpr int kNumBars = 19;
+constexpr int kQOff = kVOff + kTileBytes;                  // Q half-tiles
+constexpr int kdOOff = kQOff + kQSlots * kHalfBytes;       // dO half-tiles
+constexpr int kdSOff = kdOOff + kdOSlots * kHalfBytes;     // dS^T buffers: 128 keys x 64 queries
+constexpr int kStageOff = kdSOff + kdSBufs * kTile * 128;  // the reducer's 4 KB per warp
+constexpr int kLseOff = kStageOff + 4 * 4096;              // [kQSlots][64] LSE * log2(e)
+constexpr int kDeltaOff = kLseOff + kQSlots * kStep * 4;   // [kdOSlots][64] D
+constexpr int kBarOff = kDeltaOff + kdOSlots * kStep * 4;
+constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kdOSlots + 10 + kdSBufs;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kBytes = kMiscOff + 16;
 static_assert(kBytes <= 232448, "shared memory budget");
@@ -75,19 +78,22 @@ struct Bars {
   uint32_t base;
   __device__ uint32_t kv_full() const { return base; }
   __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t q_empty(int s) const { return base + 8 * (3 + s); }
-  __device__ uint32_t do_full(int s) const { return base + 8 * (5 + s); }
-  __device__ uint32_t do_empty(int s) const { return base + 8 * (7 + s); }
-  __device__ uint32_t s_full() const { return base + 8 * 9; }
-  __device__ uint32_t p_full() const { return base + 8 * 10; }
-  __device__ uint32_t dp_full() const { return base + 8 * 11; }
-  __device__ uint32_t ds_full() const { return base + 8 * 12; }
-  __device__ uint32_t dq_full() const { return base + 8 * 13; }
-  __device__ uint32_t dq_free() const { return base + 8 * 14; }
-  __device__ uint32_t k_tmem() const { return base + 8 * 15; }  // K_j is in tensor memory
-  __device__ uint32_t acc_done() const { return base + 8 * 16; }
-  __device__ uint32_t teardown() const { return base + 8 * 17; }
-  __device__ uint32_t ds_empty() const { return base + 8 * 18; }  // dK, dQ^T have read dS^T
+  __device__ uint32_t q_empty(int s) const { return base + 8 * (1 + kQSlots + s); }
+  __device__ uint32_t do_full(int s) const { return base + 8 * (1 + 2 * kQSlots + s); }
+  __device__ uint32_t do_empty(int s) const { return base + 8 * (1 + 2 * kQSlots + kdOSlots + s); }
+  static constexpr int kX = 1 + 2 * kQSlots + 2 * kdOSlots;
+  __device__ uint32_t s_full() const { return base + 8 * (kX + 0); }
+  __device__ uint32_t p_full() const { return base + 8 * (kX + 1); }
+  __device__ uint32_t dp_full() const { return base + 8 * (kX + 2); }
+  __device__ uint32_t ds_full() const { return base + 8 * (kX + 3); }
+  __device__ uint32_t dq_full() const { return base + 8 * (kX + 4); }
+  __device__ uint32_t dq_free() const { return base + 8 * (kX + 5); }
+  __device__ uint32_t k_tmem() const { return base + 8 * (kX + 6); }  // K_j is in tensor memory
+  __device__ uint32_t acc_done() const { return base + 8 * (kX + 7); }
+  __device__ uint32_t teardown() const { return base + 8 * (kX + 8); }
+  __device__ uint32_t spare() const { return base + 8 * (kX + 9); }
+  // dK and dQ^T have read dS^T buffer b
+  __device__ uint32_t ds_empty(int b) const { return base + 8 * (kX + 10 + b); }
 };
 
 enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleInit = 5 };
@@ -120,24 +126,26 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void load_q(const BwdParams &p, const Bars &bars, int s, int i,
-                                       uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
-  mbar_arrive_expect_tx(bars.q_full(s), kTileBytes + kTile * 4);
+// Rows 128 i + 64 hs .. + 63 of Q with their LSE * log2(e) into Q slot s.
+__device__ __forceinline__ void load_qh(const BwdParams &p, const Bars &bars, int s, int i, int hs,
+                                        uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
+  mbar_arrive_expect_tx(bars.q_full(s), kHalfBytes + kStep * 4);
   for (int c = 0; c < 2; ++c)
-    tma_load_4d(s_base + kQOff + s * kTileBytes + c * kChunkBytes, &p.tm_q, c * 64, i * kTile,
-                h_idx, b_idx, bars.q_full(s));
-  bulk_load_1d(s_base + kLseOff + s * kTile * 4, p.lse2 + stat_head + (size_t)i * kTile,
-               kTile * 4, bars.q_full(s));
+    tma_load_4d(s_base + kQOff + s * kHalfBytes + c * kHalfChunk, &p.tm_qh, c * 64,
+                i * kTile + hs * kStep, h_idx, b_idx, bars.q_full(s));
+  bulk_load_1d(s_base + kLseOff + s * kStep * 4,
+               p.lse2 + stat_head + (size_t)i * kTile + hs * kStep, kStep * 4, bars.q_full(s));
 }
 
-__device__ __forceinline__ void load_do(const BwdParams &p, const Bars &bars, int s, int i,
-                                        uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
-  mbar_arrive_expect_tx(bars.do_full(s), kTileBytes + kTile * 4);
+// The same rows of dO with their D into dO slot s.
+__device__ __forceinline__ void load_doh(const BwdParams &p, const Bars &bars, int s, int i, int hs,
+                                         uint32_t s_base, size_t stat_head, int h_idx, int b_idx) {
+  mbar_arrive_expect_tx(bars.do_full(s), kHalfBytes + kStep * 4);
   for (int c = 0; c < 2; ++c)
-    tma_load_4d(s_base + kdOOff + s * kTileBytes + c * kChunkBytes, &p.tm_do, c * 64, i * kTile,
-                h_idx, b_idx, bars.do_full(s));
-  bulk_load_1d(s_base + kDeltaOff + s * kTile * 4, p.delta + stat_head + (size_t)i * kTile,
-               kTile * 4, bars.do_full(s));
+    tma_load_4d(s_base + kdOOff + s * kHalfBytes + c * kHalfChunk, &p.tm_doh, c * 64,
+                i * kTile + hs * kStep, h_idx, b_idx, bars.do_full(s));
+  bulk_load_1d(s_base + kDeltaOff + s * kStep * 4,
+               p.delta + stat_head + (size_t)i * kTile + hs * kStep, kStep * 4, bars.do_full(s));
 }
 
 template <bool kF16>
@@ -153,6 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t sK = s_base + kKOff, sV = s_base + kVOff;
   const uint32_t sQ = s_base + kQOff, sdO = s_base + kdOOff, sdS = s_base + kdSOff;
+  // slots and buffers of step s
+  auto q_slot = [](int s) { return s % kQSlots; };
+  auto do_slot = [](int s) { return s % kdOSlots; };
   const float *lse_s = reinterpret_cast<const float *>(smem + kLseOff);
   const float *delta_s = reinterpret_cast<const float *>(smem + kDeltaOff);
   Bars bars{s_base + kBarOff};
@@ -180,12 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.q_full(s), 1);
       mbar_init(bars.q_empty(s), 1);
     }
-    // a dO slot is free once the second step of its Q tile has had dV
-    // (one commit) and the softmax warps have read D_i (256 threads)
+    // a dO slot is free once dV of its step has read it (one commit) and the
+    // softmax warps have read D (256 threads)
     for (int s = 0; s < kdOSlots; ++s) {
       mbar_init(bars.do_full(s), 1);
       mbar_init(bars.do_empty(s), 257);
     }
+    for (int b = 0; b < kdSBufs; ++b) mbar_init(bars.ds_empty(b), 1);
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.p_full(), 256);
     mbar_init(bars.dp_full(), 1);
@@ -195,21 +207,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.k_tmem(), 128);
     mbar_init(bars.acc_done(), 1);
     mbar_init(bars.teardown(), 1);
-    mbar_init(bars.ds_empty(), 1);
+    mbar_init(bars.spare(), 1);
     misc[2] = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_qh);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
-    tma_prefetch_desc(&p.tm_do);
+    tma_prefetch_desc(&p.tm_doh);
+    tma_prefetch_desc(&p.tm_dqacc);
     if (any && !(p.debug_flags & kDebugSkipLoads)) {
       mbar_arrive_expect_tx(bars.kv_full(), 2 * kTileBytes);
       for (int c = 0; c < 2; ++c) {
         tma_load_4d(sK + c * kChunkBytes, &p.tm_k, c * 64, j * kTile, h_idx, b_idx, bars.kv_full());
         tma_load_4d(sV + c * kChunkBytes, &p.tm_v, c * 64, j * kTile, h_idx, b_idx, bars.kv_full());
       }
-      load_q(p, bars, 0, first, s_base, stat_head, h_idx, b_idx);
-      load_do(p, bars, 0, first, s_base, stat_head, h_idx, b_idx);
+      load_qh(p, bars, 0, first, 0, s_base, stat_head, h_idx, b_idx);
+      load_doh(p, bars, 0, first, 0, s_base, stat_head, h_idx, b_idx);
     }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
@@ -221,24 +234,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
   if (warp == 0) {
-    // ---- TMA producer ------------------------------------------------------
+    // ---- TMA producer: Q and dO half-tiles, one per step ------------------------
     if (elect_one() && any && !(p.debug_flags & kDebugSkipLoads)) {
-      int nq = 1, ndo = 1;
+      int nq = 1, ndo = 1;  // halves issued: the first step's came with the set-up
       bool ok = true;
-      for (int i = next_q(sh, first + 1, j); i < T && ok; i = next_q(sh, i + 1, j)) {
-        const int qs = nq % kQSlots;
-        ok = mbar_wait(bars.q_empty(qs), ((nq / kQSlots) & 1u) ^ 1u, st,
-                       status_code(kKernBwdFused, kRoleLoad, 1));
-        if (!ok) break;
-        load_q(p, bars, qs, i, s_base, stat_head, h_idx, b_idx);
-        ++nq;
-        const int ds = ndo % kdOSlots;
-        ok = mbar_wait(bars.do_empty(ds), ((ndo / kdOSlots) & 1u) ^ 1u, st,
-                       status_code(kKernBwdFused, kRoleLoad, 4));
-        if (!ok) break;
-        load_do(p, bars, ds, i, s_base, stat_head, h_idx, b_idx);
-        ++ndo;
+      for (int i = first; i < T && ok; i = next_q(sh, i + 1, j)) {
+        for (int hs = (i == first ? 1 : 0); hs < 2 && ok; ++hs) {
+          const int qs = nq % kQSlots;
+          ok = mbar_wait(bars.q_empty(qs), ((nq / kQSlots) & 1u) ^ 1u, st,
+                         status_code(kKernBwdFused, kRoleLoad, 1));
+          if (!ok) break;
+          load_qh(p, bars, qs, i, hs, s_base, stat_head, h_idx, b_idx);
+          ++nq;
+          const int ds = ndo % kdOSlots;
+          ok = mbar_wait(bars.do_empty(ds), ((ndo / kdOSlots) & 1u) ^ 1u, st,
+                         status_code(kKernBwdFused, kRoleLoad, 4));
+          if (!ok) break;
+          load_doh(p, bars, ds, i, hs, s_base, stat_head, h_idx, b_idx);
+          ++ndo;
+        }
       }
+      // teardown: every copy issued has landed
       mbar_wait_drain(bars.kv_full(), 0, st, status_code(kKernBwdFused, kRoleLoad, 2));
       for (int s = 0; s < kQSlots && s < nq; ++s) {
         const int last = s + ((nq - 1 - s) / kQSlots) * kQSlots;
@@ -260,88 +276,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDq = idesc_f32acc(kD, 64, 1, 1, kF16);       // dQ^T: A, B MN-major
       bool ok = !any || (mbar_wait(bars.kv_full(), 0, st, status_code(kKernBwdFused, kRoleMma, 1)) &&
                          mbar_wait(bars.k_tmem(), 0, st, status_code(kKernBwdFused, kRoleMma, 11)));
-      // S^T = K Q^T over the 64 queries 64hs.. of Q slot qs: A = K in tensor
-      // memory (8 columns per 16-element K-step), B = Q rows (K-major)
-      auto issue_s = [&](int qs, int hs) {
+      // S^T = K Q^T over a step's 64 queries (Q slot qs): A = K in tensor
+      // memory (8 columns per 16-element K-step), B = the Q rows (K-major)
+      auto issue_s = [&](int qs) {
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_f16kind_ts(tmem + kColS, tmem + kColK + kk * 8,
-                         sdesc_sw128(sQ + qs * kTileBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32 +
-                                         hs * 64 * 128, 16, 1024),
+                         sdesc_sw128(sQ + qs * kHalfBytes + (kk >> 2) * kHalfChunk + (kk & 3) * 32,
+                                     16, 1024),
                          kIdS, kk > 0);
       };
-      // dP^T = V dO^T over the step's 64 queries: both operands K-major
-      auto issue_dp = [&](int ds, int hs) {
+      // dP^T = V dO^T over a step's 64 queries (dO slot ds): both K-major
+      auto issue_dp = [&](int ds) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_f16kind_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
-                         sdesc_sw128(sdO + ds * kTileBytes + off + hs * 64 * 128, 16, 1024), kIdS,
-                         kk > 0);
-        }
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_f16kind_ss(tmem + kColDP,
+                         sdesc_sw128(sV + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
+                         sdesc_sw128(sdO + ds * kHalfBytes + (kk >> 2) * kHalfChunk + (kk & 3) * 32,
+                                     16, 1024),
+                         kIdS, kk > 0);
       };
-      // acc += X Y: X packed in tensor memory at a_col (queries 32h.. of the
-      // step at a_col + 32h), Y = the step's 64 rows (MN-major, 16 per K-step)
-      auto issue_acc = [&](uint32_t a_col, uint32_t y_base, int hs, uint32_t col, bool first_step) {
+      // dV += P^T dO: P^T packed in tensor memory (queries 32h.. of the step
+      // at kColS + 32h), dO rows of the step's slot (MN-major, 16 per K-step)
+      auto issue_dv = [&](int ds, bool first_step) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16kind_ts(tmem + col, tmem + a_col + (kk >> 1) * 32 + (kk & 1) * 8,
-                         sdesc_sw128(y_base + (4 * hs + kk) * 2048, kChunkBytes, 1024), kIdAcc,
+          mma_f16kind_ts(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8,
+                         sdesc_sw128(sdO + ds * kHalfBytes + kk * 2048, kHalfChunk, 1024), kIdAcc,
                          (!first_step || kk > 0) ? 1u : 0u);
       };
-      // dK += dS^T Q over the step's 64 queries: A = the dS^T tile (K-major:
-      // rows = keys), B = Q rows (MN-major)
-      auto issue_dk = [&](uint32_t q_base, int hs, bool first_step) {
+      // dK += dS^T Q: A = dS^T buffer b (K-major: rows = keys), B = the Q rows
+      // of the step's slot (MN-major)
+      auto issue_dk = [&](int b, int qs, bool first_step) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16kind_ss(tmem + kColDK, sdesc_sw128(sdS + kk * 32, 16, 1024),
-                         sdesc_sw128(q_base + (4 * hs + kk) * 2048, kChunkBytes, 1024), kIdAcc,
+          mma_f16kind_ss(tmem + kColDK, sdesc_sw128(sdS + b * kChunkBytes + kk * 32, 16, 1024),
+                         sdesc_sw128(sQ + qs * kHalfBytes + kk * 2048, kHalfChunk, 1024), kIdAcc,
                          (!first_step || kk > 0) ? 1u : 0u);
       };
       // dQ^T = K^T dS^T: A = K_j read MN-major (M = head dimension along a
-      // row, K = keys down the rows), B = the dS^T tile (N = 64 queries along
+      // row, K = keys down the rows), B = dS^T buffer b (N = 64 queries along
       // a row, K = keys)
-      auto issue_dq = [&]() {
+      auto issue_dq = [&](int b) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_f16kind_ss(tmem + kColDQ, sdesc_sw128(sK + kk * 2048, kChunkBytes, 1024),
-                         sdesc_sw128(sdS + kk * 2048, kChunkBytes, 1024), kIdDq, kk > 0);
+                         sdesc_sw128(sdS + b * kChunkBytes + kk * 2048, kChunkBytes, 1024), kIdDq,
+                         kk > 0);
       };
       if (ok && any) {
         ok = mbar_wait(bars.q_full(0), 0, st, status_code(kKernBwdFused, kRoleMma, 2));
         if (ok) {
           tc_fence_after();
-          issue_s(0, 0);
+          issue_s(0);
           mma_commit(bars.s_full());
           ok = mbar_wait(bars.do_full(0), 0, st, status_code(kKernBwdFused, kRoleMma, 7));
         }
         if (ok) {
           tc_fence_after();
-          issue_dp(0, 0);
+          issue_dp(0);
           mma_commit(bars.dp_full());
         }
       }
-      int n = 0, s = 0, qs = 0, qph = 0;  // Q tile count, step count, Q slot and its phase
-      for (int i = first; i < T && ok; ++n) {
-        const int ds = n & 1, ds1 = ds ^ 1;
-        const int qs1 = qs + 1 == kQSlots ? 0 : qs + 1;
-        const int qph1 = qs + 1 == kQSlots ? qph ^ 1 : qph;
+      int s = 0;  // steps: 64 queries each, two per Q tile
+      for (int i = first; i < T && ok;) {
         const int inext = next_q(sh, i + 1, j);
         for (int hs = 0; hs < 2 && ok; ++hs, ++s) {
-          const bool second = hs == 1;
-          const bool more = !second || inext < T;  // a step s + 1 follows
+          const bool more = hs == 0 || inext < T;  // a step s + 1 follows
+          const int b = s & 1;                     // dS^T buffer of step s
           ok = mbar_wait(bars.p_full(), s & 1, st, status_code(kKernBwdFused, kRoleMma, 3));
           if (!ok) break;
           tc_fence_after();
-          issue_acc(kColS, sdO + ds * kTileBytes, hs, kColDV, s == 0);
-          if (second) mma_commit(bars.do_empty(ds));  // dV and dP^T are done with dO_i
+          issue_dv(do_slot(s), s == 0);
+          mma_commit(bars.do_empty(do_slot(s)));  // dP^T(s) and dV(s) are done with dO
           if (more) {
-            if (second) {
-              ok = mbar_wait(bars.q_full(qs1), qph1, st, status_code(kKernBwdFused, kRoleMma, 4));
-              if (!ok) break;
-              tc_fence_after();
-            }
-            issue_s(second ? qs1 : qs, second ? 0 : 1);
+            ok = mbar_wait(bars.q_full(q_slot(s + 1)), ((s + 1) / kQSlots) & 1, st,
+                           status_code(kKernBwdFused, kRoleMma, 4));
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(q_slot(s + 1));
             mma_commit(bars.s_full());
           }
           ok = mbar_wait(bars.ds_full(), s & 1, st, status_code(kKernBwdFused, kRoleMma, 5));
@@ -349,29 +362,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // the softmax warps have read dP^T(s): dP^T(s+1) may take its columns
           if (more) {
-            if (second) {
-              ok = mbar_wait(bars.do_full(ds1), ((n + 1) >> 1) & 1, st,
-                             status_code(kKernBwdFused, kRoleMma, 7));
-              if (!ok) break;
-              tc_fence_after();
-            }
-            issue_dp(second ? ds1 : ds, second ? 0 : 1);
+            ok = mbar_wait(bars.do_full(do_slot(s + 1)), ((s + 1) / kdOSlots) & 1, st,
+                           status_code(kKernBwdFused, kRoleMma, 7));
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(do_slot(s + 1));
             mma_commit(bars.dp_full());
           }
-          issue_dk(sQ + qs * kTileBytes, hs, s == 0);
-          if (second) mma_commit(bars.q_empty(qs));  // S^T and dK are done with Q_i
+          issue_dk(b, q_slot(s), s == 0);
+          mma_commit(bars.q_empty(q_slot(s)));  // S^T(s) and dK(s) are done with Q
           if (s > 0) {  // the reducer has read dQ^T(s-1)
             ok = mbar_wait(bars.dq_free(), (s - 1) & 1, st, status_code(kKernBwdFused, kRoleMma, 10));
             if (!ok) break;
             tc_fence_after();
           }
-          issue_dq();
+          issue_dq(b);
           mma_commit(bars.dq_full());
-          mma_commit(bars.ds_empty());  // dK(s) and dQ^T(s) have read dS^T(s)
+          mma_commit(bars.ds_empty(b));  // dK(s) and dQ^T(s) have read dS^T buffer b
         }
         i = inext;
-        qs = qs1;
-        qph = qph1;
       }
       if (ok) mma_commit(bars.acc_done());
       mma_commit(bars.teardown());
@@ -405,18 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bars.k_tmem());
       }
     }
-    int n = 0, s = 0, qs = 0, qph = 0;
-    for (int i = first; i < T && ok; i = next_q(sh, i + 1, j), ++n) {
-      const int ds = n & 1;
-      const float *lse2 = lse_s + qs * kTile;
-      const float *delta = delta_s + ds * kTile;
+    int s = 0;  // steps: 64 queries each, two per Q tile
+    for (int i = first; i < T && ok; i = next_q(sh, i + 1, j)) {
       const bool cross = sh.causal && kTile * j + kTile - 1 > kTile * i + sh.causal_off;
       for (int hs = 0; hs < 2 && ok; ++hs, ++s) {
         const int q0 = 64 * hs + 32 * h;  // this warpgroup's first query of the step in Q tile i
+        const float *lse2 = lse_s + q_slot(s) * kStep + 32 * h;
+        const float *delta = delta_s + do_slot(s) * kStep + 32 * h;
         ok = __all_sync(0xffffffffu, mbar_wait(bars.s_full(), s & 1, st,
                                                status_code(kKernBwdFused, kRoleSoftmax, 1)));
-        if (ok && hs == 0)
-          ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full(qs), qph, st,
+        if (ok)
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full(q_slot(s)), (s / kQSlots) & 1, st,
                                                  status_code(kKernBwdFused, kRoleSoftmax, 2)));
         if (!ok) break;
         tc_fence_after();
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int x = 0; x < 32; ++x)
-            pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x]), c, -lse2[q0 + x]));
+            pr[x] = ex2_approx(fmaf(__uint_as_float(sr[x]), c, -lse2[x]));
           if (cross) {  // key kr sees query q0 + x only if x >= lo
             const int lo = kTile * (j - i) + kr - sh.causal_off - q0;
 #pragma unroll
@@ -444,13 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(bars.p_full());
         }
-        // dS^T_kq = P^T_kq (dP^T_kq - D_q) into the shared dS^T tile (the A
+        // dS^T_kq = P^T_kq (dP^T_kq - D_q) into dS^T buffer s & 1 (the A
         // operand of dK, the B operand of dQ^T): row kr, queries 32h.. of the
         // step = 16-byte pieces 4h..4h+3
         ok = __all_sync(0xffffffffu, mbar_wait(bars.dp_full(), s & 1, st,
                                                status_code(kKernBwdFused, kRoleSoftmax, 4)));
-        if (ok && hs == 0)
-          ok = __all_sync(0xffffffffu, mbar_wait(bars.do_full(ds), (n >> 1) & 1, st,
+        if (ok)
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.do_full(do_slot(s)), (s / kdOSlots) & 1, st,
                                                  status_code(kKernBwdFused, kRoleSoftmax, 5)));
         if (!ok) break;
         tc_fence_after();
@@ -461,17 +469,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int x = 0; x < 32; x += 2)
-            dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x]) - delta[q0 + x]),
-                                     pr[x + 1] * (__uint_as_float(dr[x + 1]) - delta[q0 + x + 1]));
+            dsp[x / 2] = pack2<kF16>(pr[x] * (__uint_as_float(dr[x]) - delta[x]),
+                                     pr[x + 1] * (__uint_as_float(dr[x + 1]) - delta[x + 1]));
         }
-        // dK(s-1) and dQ^T(s-1) have read the tile
-        if (s > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bars.ds_empty(), (s - 1) & 1, st,
+        // dK(s-2) and dQ^T(s-2) have read the buffer
+        if (s >= kdSBufs) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.ds_empty(s & 1), ((s >> 1) - 1) & 1, st,
                                                  status_code(kKernBwdFused, kRoleSoftmax, 7)));
           if (!ok) break;
         }
         {
-          const uint32_t row = sdS + kr * 128;
+          const uint32_t row = sdS + (s & 1) * kChunkBytes + kr * 128;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             st_shared_v4(row + ((uint32_t(4 * h + u) ^ uint32_t(kr & 7)) << 4), dsp[4 * u],
@@ -480,10 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // the tensor core reads dS^T through the async proxy
         tc_fence_before();         // dP^T(s) has been read: dP^T(s+1) may take its columns
         mbar_arrive(bars.ds_full());
-        if (hs == 1) mbar_arrive(bars.do_empty(ds));  // D_i has been read
+        mbar_arrive(bars.do_empty(do_slot(s)));  // D has been read
       }
-      qph = qs + 1 == kQSlots ? qph ^ 1 : qph;
-      qs = qs + 1 == kQSlots ? 0 : qs + 1;
     }
     // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled), through the
     // K_j and V_j buffers once every MMA has completed

@@ -107,6 +107,7 @@ struct BwdParams {
   CUtensorMap tm_dq, tm_dk, tm_dv;     // maps over the gradients, 64 x 32 boxes (TMA stores)
   CUtensorMap tm_dqacc;                // one-pass backward at d = 128: 2-D map over dq_acc
                                        // ([rows][128] fp32), 32 x 32 boxes, 128-byte swizzle
+  CUtensorMap tm_qh, tm_doh;           // one-pass backward at d = 128: Q and dO with 64-row boxes
   Shape sh;
   const void *o, *dout;               // 16-bit rows, strides so / sdo
   RowStrides so, sdo;
