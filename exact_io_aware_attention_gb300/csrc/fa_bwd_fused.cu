@@ -152,15 +152,6 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_
                : "memory");
 }
 
-template <uint32_t kRegs>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
 // This thread's row of 32 fp32 values into a 4 KB chunk slot (32 rows x 128
 // bytes, 16-byte pieces swizzled by row & 7, so that neither this write nor
 // the read-back by rows conflicts on shared-memory banks).
@@ -681,6 +672,7 @@ cudaError_t launch_fused_d(const BwdParams &p, cudaStream_t stream) {
     if (!configured) {
       e = cudaFuncSetAttribute(fa_bwd_fused<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                L::kBytes);
+      if (e == cudaSuccess) e = check_kernel_regs(fa_bwd_fused<D, kF16>, 65536 / kThreads);
       if (e != cudaSuccess) return e;
       configured = true;
     }

@@ -49,6 +49,19 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 384;
+// registers per thread: the launch bound (65536 / 384, rounded down to 8) and
+// the split of it between the warpgroups
+constexpr int kRegsLaunch = 168;
+template <int D>
+constexpr int kRegsLoadMma = 88;
+template <int D>
+constexpr int kRegsSoftmax = 208;
+static_assert(kRegsLoadMma<64> * 128 + kRegsSoftmax<64> * 256 == kRegsLaunch * kThreads,
+              "warpgroup register split");
+static_assert(kRegsLoadMma<96> * 128 + kRegsSoftmax<96> * 256 == kRegsLaunch * kThreads,
+              "warpgroup register split");
+static_assert(kRegsLoadMma<128> * 128 + kRegsSoftmax<128> * 256 == kRegsLaunch * kThreads,
+              "warpgroup register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
 template <int D>
@@ -61,8 +74,9 @@ struct FwdLayout {
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
   static constexpr int kListOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2][2], o_done[2], teardown
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 4 + 2 + 1;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2][2], o_done[2], teardown,
+  // s_read[2], pv_done[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 4 + 2 + 1 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 32;
   static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
@@ -85,6 +99,10 @@ struct Bars {
   __device__ uint32_t p_full(int t, int u) const { return base + 8 * ((u ? 8 : 3) + 2 * stages + t); }
   __device__ uint32_t o_done(int t) const { return base + 8 * (5 + 2 * stages + t); }
   __device__ uint32_t teardown() const { return base + 8 * (7 + 2 * stages); }
+  // d = 64: the softmax warps of Q tile t have read S_t (128 arrivals), and
+  // PV_t has completed, so its P_t columns may be rewritten
+  __device__ uint32_t s_read(int t) const { return base + 8 * (10 + 2 * stages + t); }
+  __device__ uint32_t pv_done(int t) const { return base + 8 * (12 + 2 * stages + t); }
 };
 
 // list entry: bits 0-11 key tile j; bits 12/13: Q tile 0/1 needs element-wise
@@ -103,6 +121,10 @@ enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 template <int D, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
+  // d = 64 moves registers between the warpgroups (setmaxnreg, below), and
+  // then every wait and store is inlined
+  constexpr bool kMoveRegs = D == 64;
+  constexpr bool kInline = true;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -146,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     for (int t = 0; t < 2; ++t) mbar_init(bars.o_done(t), 1);
     mbar_init(bars.teardown(), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_read(t), 128);
+      mbar_init(bars.pv_done(t), 1);
+    }
     misc[2] = 0;
     misc[6] = bh;
     fence_mbar_init();
@@ -252,137 +278,170 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int count = misc[1];
+  // d = 64: registers per thread by warpgroup, 88 for the producer / MMA
+  // warpgroup and 208 for each softmax warpgroup (88 * 128 + 208 * 256 =
+  // 168 * 384, the launch's total), which keeps the softmax loop free of
+  // spills; at d >= 96 the MMA issuer, with twice the MMAs per step, runs
+  // slower with fewer registers and the split is not made. Every call below is
+  // inlined: an out-of-line call in a kernel with its own register counts is
+  // not compiled.
+  if (warp < 4) {
+    if constexpr (kMoveRegs) setmaxnreg_dec<kRegsLoadMma<D>>();
+    if (warp == 0) {
+      // ---- TMA producer ------------------------------------------------------
+      if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
+        int pos = misc[3];  // K and V of list[0] may have been issued during set-up
+        bool ok = true;
+        for (int n = pos / 2; n < count && ok; ++n) {
+          const int kvrow = entry_j(list[n]) * kTile;
+          for (int which = 0; which < 2 && ok; ++which, ++pos) {
+            const int s = pos % L::kStages;
+            const uint32_t u = pos / L::kStages;
+            ok = mbar_wait_t<kInline>(bars.kv_empty(s), (u & 1u) ^ 1u, st, status_code(kKernFwd, kRoleLoad, 1));
+            if (!ok) break;
+            mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+            const CUtensorMap *tm = which ? &p.tm_v : &p.tm_k;
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_4d(sKV + s * L::kTileBytes + c * L::kChunkBytes, tm, c * 64, kvrow, h_idx,
+                          b_idx, bars.kv_full(s));
+          }
+        }
+        // teardown: wait (bounded) until every copy issued has landed (the Q
+        // tiles were loaded during set-up)
+        mbar_wait_drain_t<kInline>(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+        for (int s = 0; s < L::kStages && s < pos; ++s) {
+          const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
+          mbar_wait_drain_t<kInline>(bars.kv_full(s), (last / L::kStages) & 1u, st,
+                    status_code(kKernFwd, kRoleLoad, 3));
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---- tcgen05 issuer ----------------------------------------------------
+      if (elect_one()) {
+        constexpr uint32_t kIdS = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // Q K^T, both K-major
+        constexpr uint32_t kIdPV = idesc_f32acc(kTile, D, 0, 1, kF16);     // P V, V is MN-major
+        bool ok = count == 0 || mbar_wait_t<kInline>(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
+        uint32_t pcount[2] = {0, 0};
+        bool first_pv[2] = {true, true};
+        // d = 64: P_t has tensor-memory columns of its own, so S_t(n+1) waits
+        // only until the softmax warps have read S_t(n) (s_read) and is issued
+        // ahead of PV_t(n): the tensor core computes it while P_t(n) is formed,
+        // which shortens the chain S -> P -> PV of a Q tile that runs alone
+        // (block-sparse masks, causal edges)
+        constexpr bool kEarlyS = D == 64 && !kSplit;
+        uint32_t s_issued[2] = {0, 0};
+        // misc[4 + t]: the last list entry Q tile t is active in (from warp 2)
 
-  if (warp == 0) {
-    // ---- TMA producer ------------------------------------------------------
-    if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
-      int pos = misc[3];  // K and V of list[0] may have been issued during set-up
-      bool ok = true;
-      for (int n = pos / 2; n < count && ok; ++n) {
-        const int kvrow = entry_j(list[n]) * kTile;
-        for (int which = 0; which < 2 && ok; ++which, ++pos) {
-          const int s = pos % L::kStages;
-          const uint32_t u = pos / L::kStages;
-          ok = mbar_wait(bars.kv_empty(s), (u & 1u) ^ 1u, st, status_code(kKernFwd, kRoleLoad, 1));
+        auto issue_s = [&](int t, int kslot) {
+          const uint32_t q_base = sQ + t * L::kTileBytes;
+          const uint32_t k_base = sKV + kslot * L::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+            mma_f16kind_ss(tmem + t * kTile, sdesc_sw128(q_base + off, 16, 1024),
+                        sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
+          }
+        };
+        // O_t += P_t V: A = P_t from tensor memory (8 columns per 16 keys),
+        // B = V with keys as K (MN-major, 16 key rows per step). With d = 128,
+        // S_t(n+1) is issued after this MMA into the columns P_t occupies; MMAs
+        // issued by one thread execute in issue order, so P_t is read first.
+        // (keys 64u .. 64u + 63: half u of P_t)
+        auto issue_pv = [&](int t, int vslot, bool first, int u) {
+          const uint32_t v_base = sKV + vslot * L::kTileBytes;
+  #pragma unroll
+          for (int kk = 4 * u; kk < 4 * u + 4; ++kk)
+            mma_f16kind_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
+                        sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
+                        (kk > 0 || !first) ? 1u : 0u);
+        };
+
+        if (ok && count > 0) {
+          // prologue: S for the first K tile
+          ok = mbar_wait_t<kInline>(bars.kv_full(0), 0, st, status_code(kKernFwd, kRoleMma, 2));
+          if (ok) {
+            tc_fence_after();
+            const uint32_t e = list[0];
+            for (int t = 0; t < 2; ++t)
+              if (entry_act(e, t)) {
+                issue_s(t, 0);
+                mma_commit(bars.s_full(t));
+                ++s_issued[t];
+              }
+            mma_commit(bars.kv_empty(0));
+          }
+        }
+        for (int n = 0; n < count && ok; ++n) {
+          const uint32_t e = list[n];
+          const int vpos = 2 * n + 1, kpos = 2 * n + 2;
+          const int vslot = vpos % L::kStages, kslot = kpos % L::kStages;
+          const bool has_next = n + 1 < count;
+          const uint32_t en = has_next ? list[n + 1] : 0u;
+          ok = mbar_wait_t<kInline>(bars.kv_full(vslot), (vpos / L::kStages) & 1u, st,
+                         status_code(kKernFwd, kRoleMma, 3));
+          if (ok && has_next)
+            ok = mbar_wait_t<kInline>(bars.kv_full(kslot), (kpos / L::kStages) & 1u, st,
+                           status_code(kKernFwd, kRoleMma, 4));
           if (!ok) break;
-          mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
-          const CUtensorMap *tm = which ? &p.tm_v : &p.tm_k;
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_4d(sKV + s * L::kTileBytes + c * L::kChunkBytes, tm, c * 64, kvrow, h_idx,
-                        b_idx, bars.kv_full(s));
-        }
-      }
-      // teardown: wait (bounded) until every copy issued has landed (the Q
-      // tiles were loaded during set-up)
-      mbar_wait_drain(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
-      for (int s = 0; s < L::kStages && s < pos; ++s) {
-        const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
-        mbar_wait_drain(bars.kv_full(s), (last / L::kStages) & 1u, st,
-                  status_code(kKernFwd, kRoleLoad, 3));
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---- tcgen05 issuer ----------------------------------------------------
-    if (elect_one()) {
-      constexpr uint32_t kIdS = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // Q K^T, both K-major
-      constexpr uint32_t kIdPV = idesc_f32acc(kTile, D, 0, 1, kF16);     // P V, V is MN-major
-      bool ok = count == 0 || mbar_wait(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
-      uint32_t pcount[2] = {0, 0};
-      bool first_pv[2] = {true, true};
-      // misc[4 + t]: the last list entry Q tile t is active in (from warp 2)
-
-      auto issue_s = [&](int t, int kslot) {
-        const uint32_t q_base = sQ + t * L::kTileBytes;
-        const uint32_t k_base = sKV + kslot * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_f16kind_ss(tmem + t * kTile, sdesc_sw128(q_base + off, 16, 1024),
-                      sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
-        }
-      };
-      // O_t += P_t V: A = P_t from tensor memory (8 columns per 16 keys),
-      // B = V with keys as K (MN-major, 16 key rows per step). With d = 128,
-      // S_t(n+1) is issued after this MMA into the columns P_t occupies; MMAs
-      // issued by one thread execute in issue order, so P_t is read first.
-      // (keys 64u .. 64u + 63: half u of P_t)
-      auto issue_pv = [&](int t, int vslot, bool first, int u) {
-        const uint32_t v_base = sKV + vslot * L::kTileBytes;
-#pragma unroll
-        for (int kk = 4 * u; kk < 4 * u + 4; ++kk)
-          mma_f16kind_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
-                      sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
-                      (kk > 0 || !first) ? 1u : 0u);
-      };
-
-      if (ok && count > 0) {
-        // prologue: S for the first K tile
-        ok = mbar_wait(bars.kv_full(0), 0, st, status_code(kKernFwd, kRoleMma, 2));
-        if (ok) {
           tc_fence_after();
-          const uint32_t e = list[0];
-          for (int t = 0; t < 2; ++t)
-            if (entry_act(e, t)) {
-              issue_s(t, 0);
-              mma_commit(bars.s_full(t));
-            }
-          mma_commit(bars.kv_empty(0));
-        }
-      }
-      for (int n = 0; n < count && ok; ++n) {
-        const uint32_t e = list[n];
-        const int vpos = 2 * n + 1, kpos = 2 * n + 2;
-        const int vslot = vpos % L::kStages, kslot = kpos % L::kStages;
-        const bool has_next = n + 1 < count;
-        const uint32_t en = has_next ? list[n + 1] : 0u;
-        ok = mbar_wait(bars.kv_full(vslot), (vpos / L::kStages) & 1u, st,
-                       status_code(kKernFwd, kRoleMma, 3));
-        if (ok && has_next)
-          ok = mbar_wait(bars.kv_full(kslot), (kpos / L::kStages) & 1u, st,
-                         status_code(kKernFwd, kRoleMma, 4));
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (entry_act(e, t)) {
-            // PV_t in two halves: the first runs while the softmax warps
-            // form the second half of P_t (the split-key instantiation waits
-            // for all of P_t on p_full(t, 1))
-            if constexpr (!kSplit) {
-              ok = mbar_wait(bars.p_full(t, 0), pcount[t] & 1u, st,
-                             status_code(kKernFwd, kRoleMma, 5 + t));
+          if constexpr (kEarlyS) {
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (!(has_next && entry_act(en, t))) continue;
+              // the previous S_t has been read out of its columns
+              ok = mbar_wait_t<kInline>(bars.s_read(t), (s_issued[t] - 1) & 1u, st,
+                                 status_code(kKernFwd, kRoleMma, 11 + t));
               if (!ok) break;
               tc_fence_after();
-              issue_pv(t, vslot, first_pv[t], 0);
+              issue_s(t, kslot);
+              mma_commit(bars.s_full(t));
+              ++s_issued[t];
             }
-            ok = mbar_wait(bars.p_full(t, 1), pcount[t] & 1u, st,
-                           status_code(kKernFwd, kRoleMma, 9 + t));
             if (!ok) break;
-            ++pcount[t];
-            tc_fence_after();
-            if constexpr (kSplit) issue_pv(t, vslot, first_pv[t], 0);
-            issue_pv(t, vslot, first_pv[t], 1);
-            first_pv[t] = false;
-            // O_t is final once this entry's PV has completed: under causal
-            // masking Q tile 0 usually ends one K/V tile before Q tile 1, and
-            // its epilogue then overlaps tile 1's last step
-            if (n == *reinterpret_cast<volatile int *>(&misc[4 + t])) mma_commit(bars.o_done(t));
           }
-          if (has_next && entry_act(en, t)) {
-            issue_s(t, kslot);
-            mma_commit(bars.s_full(t));
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (entry_act(e, t)) {
+              // PV_t in two halves: the first runs while the softmax warps
+              // form the second half of P_t (the split-key instantiation waits
+              // for all of P_t on p_full(t, 1))
+              if constexpr (!kSplit) {
+                ok = mbar_wait_t<kInline>(bars.p_full(t, 0), pcount[t] & 1u, st,
+                               status_code(kKernFwd, kRoleMma, 5 + t));
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, vslot, first_pv[t], 0);
+              }
+              ok = mbar_wait_t<kInline>(bars.p_full(t, 1), pcount[t] & 1u, st,
+                             status_code(kKernFwd, kRoleMma, 9 + t));
+              if (!ok) break;
+              ++pcount[t];
+              tc_fence_after();
+              if constexpr (kSplit) issue_pv(t, vslot, first_pv[t], 0);
+              issue_pv(t, vslot, first_pv[t], 1);
+              first_pv[t] = false;
+              // O_t is final once this entry's PV has completed: under causal
+              // masking Q tile 0 usually ends one K/V tile before Q tile 1, and
+              // its epilogue then overlaps tile 1's last step
+              if (n == *reinterpret_cast<volatile int *>(&misc[4 + t])) mma_commit(bars.o_done(t));
+              if constexpr (kEarlyS) mma_commit(bars.pv_done(t));
+            }
+            if (!kEarlyS && has_next && entry_act(en, t)) {
+              issue_s(t, kslot);
+              mma_commit(bars.s_full(t));
+            }
           }
+          if (!ok) break;
+          mma_commit(bars.kv_empty(vslot));
+          if (has_next) mma_commit(bars.kv_empty(kslot));
         }
-        if (!ok) break;
-        mma_commit(bars.kv_empty(vslot));
-        if (has_next) mma_commit(bars.kv_empty(kslot));
+        // teardown: every MMA this thread issued has completed
+        mma_commit(bars.teardown());
+        mbar_wait_drain_t<kInline>(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
       }
-      // teardown: every MMA this thread issued has completed
-      mma_commit(bars.teardown());
-      mbar_wait_drain(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= 4) {
+  } else {
+    if constexpr (kMoveRegs) setmaxnreg_inc<kRegsSoftmax<D>>();
     // ---- softmax -----------------------------------------------------------
     const int t = (warp - 4) >> 2;                 // Q tile of this warpgroup
     const int r = threadIdx.x - 128 * (1 + t);     // row within the tile = TMEM lane
@@ -400,8 +459,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       for (int n = 0; n < count; ++n) {
         const uint32_t e = list[n];
         if (!entry_act(e, t)) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.s_full(t), scount & 1u, st,
+        ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.s_full(t), scount & 1u, st,
                                                status_code(kKernFwd, kRoleSoftmax, 1 + t)));
+        // d = 64: S_t(n) was issued ahead of PV_t(n-1), so its completion no
+        // longer implies that PV_t(n-1) has read P_t and written O_t; wait for
+        // that before this step rewrites them
+        constexpr bool kEarlyS = D == 64 && !kSplit;
+        if (kEarlyS && ok && any)
+          ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.pv_done(0) + ((~threadIdx.x & 128u) >> 4),
+                                                     (scount - 1) & 1u, st,
+                                                     status_code(kKernFwd, kRoleSoftmax, 4)));
         if (!ok) break;
         ++scount;
         tc_fence_after();
@@ -409,6 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
         tmem_wait_ld();
+        if constexpr (kEarlyS) {  // S_t's columns may take S_t(n+1)
+          tc_fence_before();
+          mbar_arrive(bars.s_read(0) + ((~threadIdx.x & 128u) >> 4));
+        }
         float s[kTile];
 #pragma unroll
         for (int x = 0; x < kTile; ++x) s[x] = __uint_as_float(sr[x >> 5][x & 31]);
@@ -418,13 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int x = 0; x < kTile; ++x)
             if (x >= lim) s[x] = -INFINITY;
         }
-        // row max with 4 independent partial maxima (short dependency chains)
+        // row max with 4 independent partial maxima (short dependency chains),
+        // two new elements per three-input max
         float mp[4];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) mp[x] = s[x];
+        for (int y = 0; y < 4; ++y) mp[y] = fmaxf(s[2 * y], s[2 * y + 1]);
 #pragma unroll
-        for (int x = 4; x < kTile; ++x) mp[x & 3] = fmaxf(mp[x & 3], s[x]);
-        const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+        for (int x = 8; x < kTile; x += 8)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) mp[y] = fmax3(mp[y], s[x + 2 * y], s[x + 2 * y + 1]);
+        const float mx = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3]));
         const float m_tile = mx * c;
         const bool need = m_tile > m_used + kRescaleThreshold;
         float alpha = 1.f;
@@ -437,16 +511,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         // early announcement costs it spills at the register limit)
         const bool resc = kSplit || (any && __any_sync(0xffffffffu, need));
         // P = exp2(s*c - m) -> 16-bit pairs (keys 2x, 2x+1 in column x) in tensor
-        // memory; the row sum uses 4 independent partial sums
-        float lp[4] = {0.f, 0.f, 0.f, 0.f};
+        // memory; the scaling and the row sum on packed fp32 pairs (one
+        // instruction per two keys; the row sum in 4 independent partial sums)
+        const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_sub, -m_sub);
+        uint64_t lp2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
         uint32_t pk0[32], pk1[32];
+        auto p_pair = [&](int x, float s0, float s1) {
+          float p0, p1;
+          f2unpack(ffma2(f2pack(s0, s1), c2, nm2), p0, p1);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          lp2[x & 1] = fadd2(lp2[x & 1], f2pack(p0, p1));
+          return pack2<kF16>(p0, p1);
+        };
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const float p0 = ex2_approx(fmaf(s[2 * x], c, -m_sub));
-          const float p1 = ex2_approx(fmaf(s[2 * x + 1], c, -m_sub));
-          lp[x & 3] += p0 + p1;
-          pk0[x] = pack2<kF16>(p0, p1);
-        }
+        for (int x = 0; x < 32; ++x) pk0[x] = p_pair(x, s[2 * x], s[2 * x + 1]);
         tmem_st32(tP, pk0);
         // keys 0..63 of P_t go to the MMA now, unless this warp's rows must
         // first rescale O_t (then both halves are announced below); the
@@ -457,18 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive(bars.p_full(0, 0) + ((~threadIdx.x & 128u) >> 4));
         }
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
-          const float p1 = ex2_approx(fmaf(s[64 + 2 * x + 1], c, -m_sub));
-          lp[x & 3] += p0 + p1;
-          pk1[x] = pack2<kF16>(p0, p1);
-        }
+        for (int x = 0; x < 32; ++x) pk1[x] = p_pair(x, s[64 + 2 * x], s[64 + 2 * x + 1]);
         tmem_st32(tP + 32, pk1);
-        l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+        float lp[2];
+        f2unpack(fadd2(lp2[0], lp2[1]), lp[0], lp[1]);
+        l = l * alpha + (lp[0] + lp[1]);
         if (resc && any && __any_sync(0xffffffffu, need)) {
           // O *= alpha for this row. The PV MMA of the previous tile has
           // completed: it was issued before this S tile, whose completion we
-          // waited for.
+          // waited for (d = 64: pv_done, waited for above).
 #pragma unroll
           for (int q = 0; q < D / 16; ++q) {
             uint32_t o[16];
@@ -492,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (ok && any)
         // this warpgroup's o_done(t), its address from threadIdx (an address
         // computed from t here costs the softmax loop registers and spills)
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.o_done(0) + ((~threadIdx.x & 128u) >> 4), 0, st,
+        ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.o_done(0) + ((~threadIdx.x & 128u) >> 4), 0, st,
                                                status_code(kKernFwd, kRoleSoftmax, 3)));
       // tensor-memory loads are warp-wide; rows past the sequence end store nothing
       const int qrow = qi * kTile + r;  // query row within the head
@@ -511,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           // 16-bit O through this tile's Q buffer, which the MMAs no longer
           // read (any: its Q load has landed, since the MMAs used it; a tile
           // without keys stores its zeros directly below)
-          store_rows_tma<D, kF16>(&p.tm_o, tO, sQ + t * L::kTileBytes, r, qi * kTile, 0, inv_l,
+          store_rows_t<kInline, D, kF16>(&p.tm_o, tO, sQ + t * L::kTileBytes, r, qi * kTile, 0, inv_l,
                                   any, sh.d, sh.nq, bh_e % sh.heads, bh_e / sh.heads);
         } else {
 #pragma unroll
@@ -627,6 +703,8 @@ cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fa_fwd_kernel<D, true, kF16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e == cudaSuccess) e = check_kernel_regs(fa_fwd_kernel<D, false, kF16>, kRegsLaunch);
+    if (e == cudaSuccess) e = check_kernel_regs(fa_fwd_kernel<D, true, kF16>, kRegsLaunch);
     if (e != cudaSuccess) return e;
     configured = true;
   }

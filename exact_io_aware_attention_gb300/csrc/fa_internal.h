@@ -133,6 +133,19 @@ enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdDkdv = 2, kKindBw
 
 // Brackets one launch with CUDA events when measurement is enabled
 // (fa_profile_enable); a no-op otherwise.
+// A kernel whose warpgroups move registers between them (setmaxnreg) must be
+// compiled to exactly the register count its split assumes: with fewer, an
+// increase would wait for registers the launch never allocated. The launch
+// functions check the compiled count once per kernel and refuse to launch on
+// a mismatch (cudaErrorInvalidKernelImage).
+template <typename Kernel>
+inline cudaError_t check_kernel_regs(Kernel kernel, int expected) {
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(kernel));
+  if (e != cudaSuccess) return e;
+  return a.numRegs == expected ? cudaSuccess : cudaErrorInvalidKernelImage;
+}
+
 class LaunchProbe {
  public:
   LaunchProbe(int kind, cudaStream_t stream);

@@ -118,6 +118,16 @@ __device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, Sta
   return mbar_wait_loop(bar, parity, st, code);
 }
 
+// mbar_wait with the loop inlined (kInline) or out of line.
+template <bool kInline>
+__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, StatusSlot st,
+                                            uint32_t code) {
+  if constexpr (kInline)
+    return mbar_wait_inl(bar, parity, st, code);
+  else
+    return mbar_wait(bar, parity, st, code);
+}
+
 // Teardown wait for copies and MMAs this CTA has already issued. Unlike
 // mbar_wait it keeps waiting after another role of the CTA has given up:
 // work in flight still writes this CTA's shared and tensor memory, so the CTA
@@ -139,6 +149,28 @@ __device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parit
 static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, StatusSlot st,
                                                     uint32_t code) {
   return mbar_wait_drain_inl(bar, parity, st, code);
+}
+
+template <bool kInline>
+__device__ __forceinline__ bool mbar_wait_drain_t(uint32_t bar, uint32_t parity, StatusSlot st,
+                                                  uint32_t code) {
+  if constexpr (kInline)
+    return mbar_wait_drain_inl(bar, parity, st, code);
+  else
+    return mbar_wait_drain(bar, parity, st, code);
+}
+
+// Register count of this warp's warpgroup: every warp of a warpgroup runs the
+// same one. An increase takes registers that other warpgroups of the CTA have
+// given up with a decrease, so the counts must add up to the launch's total
+// (the kernel compiled to exactly its launch bound: see check_kernel_regs).
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ---------------------------------------------------------------------------
@@ -338,6 +370,43 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Pairs of fp32 values in one 64-bit register pair, for the packed fp32
+// arithmetic of sm_100-class GPUs (one instruction for two lanes' worth).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float lg2_approx(float x) {
