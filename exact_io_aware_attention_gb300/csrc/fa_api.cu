@@ -341,6 +341,14 @@ fa_status forward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor *
   }
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.head_group = forward_head_group(p.sh.bh, Nk, d);
+  p.sms = sm_count();
+  {
+    // FA_FWD_Q_TILES=1 or 2 fixes the Q tiles per CTA of the d = 64 forward
+    // (tuning and tests); otherwise the launch chooses
+    const char *e = getenv("FA_FWD_Q_TILES");
+    const int q = e ? atoi(e) : 0;
+    p.q_tiles = (q == 1 || q == 2) ? q : 0;
+  }
   p.debug_flags = g_debug_flags.load();
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);

@@ -48,30 +48,38 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 384;
-// registers per thread: the launch bound (65536 / 384, rounded down to 8) and
-// the split of it between the warpgroups
-constexpr int kRegsLaunch = 168;
-template <int D>
-constexpr int kRegsLoadMma = 88;
-template <int D>
-constexpr int kRegsSoftmax = 208;
-static_assert(kRegsLoadMma<64> * 128 + kRegsSoftmax<64> * 256 == kRegsLaunch * kThreads,
+// kNT Q tiles per CTA: two (the general form), or one at d = 64 without the
+// key split, where two CTAs share an SM
+template <int kNT>
+constexpr int kThreadsFor = 128 * (1 + kNT);
+template <int kNT>
+constexpr int kCtasPerSm = kNT == 1 ? 2 : 1;
+// registers per thread: the launch bound (65536 / threads per SM, rounded down
+// to 8) and, where the warpgroups move registers (d = 64), the split of it
+// between the producer / MMA warpgroup and each softmax warpgroup
+template <int kNT>
+constexpr int kRegsLaunch = kNT == 2 ? 168 : 128;
+template <int kNT>
+constexpr int kRegsLoadMma = kNT == 2 ? 88 : 56;
+template <int kNT>
+constexpr int kRegsSoftmax = kNT == 2 ? 208 : 200;
+static_assert(kRegsLoadMma<2> * 128 + kRegsSoftmax<2> * 256 == kRegsLaunch<2> * kThreadsFor<2>,
               "warpgroup register split");
-static_assert(kRegsLoadMma<96> * 128 + kRegsSoftmax<96> * 256 == kRegsLaunch * kThreads,
+static_assert(kRegsLoadMma<1> * 128 + kRegsSoftmax<1> * 128 == kRegsLaunch<1> * kThreadsFor<1>,
               "warpgroup register split");
-static_assert(kRegsLoadMma<128> * 128 + kRegsSoftmax<128> * 256 == kRegsLaunch * kThreads,
-              "warpgroup register split");
+static_assert(kRegsLaunch<1> * kThreadsFor<1> * kCtasPerSm<1> <= 65536, "registers per SM");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by > 2^8
 
-template <int D>
+template <int D, int kNT>
 struct FwdLayout {
   static constexpr int kChunks = (D + 63) / 64;       // 128-byte column chunks per row (d = 96: 2, the last half zeros)
   static constexpr int kChunkBytes = kTile * 128;     // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (kChunks == 2) ? 5 : 10;  // K/V ring slots (K and V alternate)
+  // K/V ring slots (K and V alternate); one Q tile: half of the SM's shared
+  // memory per CTA
+  static constexpr int kStages = kNT == 1 ? 5 : (kChunks == 2) ? 5 : 10;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + 2 * kTileBytes;
+  static constexpr int kKVOff = kQOff + kNT * kTileBytes;
   static constexpr int kListOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kListOff + kMaxTiles * 2;
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2][2], o_done[2], teardown,
@@ -85,7 +93,13 @@ struct FwdLayout {
   // O_t += P_t V. With d = 128 the 512 columns hold S_0, S_1, O_0, O_1 and P_t
   // takes the first half of S_t's columns once S_t has been read; with d = 64
   // it has columns of its own.
-  __host__ __device__ static constexpr uint32_t col_p(int t) { return D >= 96 ? t * kTile : 384 + 64 * t; }
+  // tensor memory: S_t at 128t, O_t after all S, P_t (d = 64) after all O;
+  // at d >= 96 P_t overlays S_t
+  static constexpr uint32_t kTmemCols = 256 * kNT;
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return kTile * kNT + t * D; }
+  __host__ __device__ static constexpr uint32_t col_p(int t) {
+    return D >= 96 ? t * kTile : kTile * kNT + kNT * D + 64 * t;
+  }
 };
 
 struct Bars {
@@ -118,9 +132,11 @@ enum Role : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 // kF16: f16 elements instead of bf16 (Q, K, V, P and a 16-bit O). D is 64, 96 or 128: at 96 the
 // tiles keep two 64-column chunks (the tensor maps read zeros in columns 96..127), the MMAs run 6
 // K-steps over the head dimension and N = 96 (the PV MMA), and 96 columns of O are stored.
-template <int D, bool kSplit, bool kF16>
-__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<D>;
+template <int D, bool kSplit, bool kF16, int kNT>
+__global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdLayout<D, kNT>;
+  static_assert(kNT == 2 || (D == 64 && !kSplit), "one Q tile per CTA: d = 64 only");
   // d = 64 moves registers between the warpgroups (setmaxnreg, below), and
   // then every wait and store is inlined
   constexpr bool kMoveRegs = D == 64;
@@ -144,14 +160,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // work item: head groups, heavy (late) Q-tile pairs first within a group;
   // the splits of one pair are adjacent, so they run together and share Q in L2
   const Shape &sh = p.sh;
-  const int npairs = (sh.tq + 1) >> 1;
+  const int npairs = kNT == 2 ? (sh.tq + 1) >> 1 : sh.tq;  // work units per head
   const int n_split = kSplit ? p.n_split : 1;
   const int split = kSplit ? int(blockIdx.x % n_split) : 0;
   const int cta = kSplit ? int(blockIdx.x / n_split) : int(blockIdx.x);
   int pair;
   const int bh = fwd_item_head(cta, sh.bh, npairs, p.head_group, &pair);
-  const int i0 = 2 * pair;
-  const bool has1 = (i0 + 1) < sh.tq;
+  const int i0 = kNT * pair;
+  const bool has1 = kNT == 2 && (i0 + 1) < sh.tq;
   const int b_idx = bh / sh.heads, h_idx = bh % sh.heads;
 
   // ---- setup -------------------------------------------------------------
@@ -214,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     misc[3] = pre;  // ring positions already issued
   } else if (warp == 1) {
-    tmem_alloc(smem_u32(&misc[0]), 512);
+    tmem_alloc(smem_u32(&misc[0]), L::kTmemCols);
     tmem_relinquish();
   } else if (warp == 2) {
     // K/V tiles visited by either Q tile, ascending, with per-tile flags
@@ -280,13 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int count = misc[1];
   // d = 64: registers per thread by warpgroup, 88 for the producer / MMA
   // warpgroup and 208 for each softmax warpgroup (88 * 128 + 208 * 256 =
-  // 168 * 384, the launch's total), which keeps the softmax loop free of
-  // spills; at d >= 96 the MMA issuer, with twice the MMAs per step, runs
-  // slower with fewer registers and the split is not made. Every call below is
+  // 168 * 384, the launch's total; one Q tile: 56 + 200 = 2 * 128), which
+  // keeps the softmax loop free of spills; at d >= 96 the MMA issuer, with
+  // twice the MMAs per step, runs slower with fewer registers and the split is
+  // not made. Every call below is
   // inlined: an out-of-line call in a kernel with its own register counts is
   // not compiled.
   if (warp < 4) {
-    if constexpr (kMoveRegs) setmaxnreg_dec<kRegsLoadMma<D>>();
+    if constexpr (kMoveRegs) setmaxnreg_dec<kRegsLoadMma<kNT>>();
     if (warp == 0) {
       // ---- TMA producer ------------------------------------------------------
       if (elect_one() && !(p.debug_flags & kDebugSkipLoads)) {
@@ -352,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const uint32_t v_base = sKV + vslot * L::kTileBytes;
   #pragma unroll
           for (int kk = 4 * u; kk < 4 * u + 4; ++kk)
-            mma_f16kind_ts(tmem + 256 + t * D, tmem + L::col_p(t) + kk * 8,
+            mma_f16kind_ts(tmem + L::col_o(t), tmem + L::col_p(t) + kk * 8,
                         sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdPV,
                         (kk > 0 || !first) ? 1u : 0u);
         };
@@ -363,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (ok) {
             tc_fence_after();
             const uint32_t e = list[0];
-            for (int t = 0; t < 2; ++t)
+            for (int t = 0; t < kNT; ++t)
               if (entry_act(e, t)) {
                 issue_s(t, 0);
                 mma_commit(bars.s_full(t));
@@ -386,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (!ok) break;
           tc_fence_after();
           if constexpr (kEarlyS) {
-            for (int t = 0; t < 2 && ok; ++t) {
+            for (int t = 0; t < kNT && ok; ++t) {
               if (!(has_next && entry_act(en, t))) continue;
               // the previous S_t has been read out of its columns
               ok = mbar_wait_t<kInline>(bars.s_read(t), (s_issued[t] - 1) & 1u, st,
@@ -399,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             }
             if (!ok) break;
           }
-          for (int t = 0; t < 2 && ok; ++t) {
+          for (int t = 0; t < kNT && ok; ++t) {
             if (entry_act(e, t)) {
               // PV_t in two halves: the first runs while the softmax warps
               // form the second half of P_t (the split-key instantiation waits
@@ -441,14 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       __syncwarp();
     }
   } else {
-    if constexpr (kMoveRegs) setmaxnreg_inc<kRegsSoftmax<D>>();
+    if constexpr (kMoveRegs) setmaxnreg_inc<kRegsSoftmax<kNT>>();
     // ---- softmax -----------------------------------------------------------
     const int t = (warp - 4) >> 2;                 // Q tile of this warpgroup
     const int r = threadIdx.x - 128 * (1 + t);     // row within the tile = TMEM lane
     const int qi = i0 + t;                         // Q tile index
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * kTile;
-    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const uint32_t tO = tmem + lane_off + L::col_o(t);
     const uint32_t tP = tmem + lane_off + L::col_p(t);
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -637,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
@@ -693,30 +710,55 @@ cudaError_t launch_combine(const FwdParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Sets the kernel's shared-memory size and checks its register count, once.
+template <int D, bool kSplit, bool kF16, int kNT>
+cudaError_t configure_fwd() {
+  static cudaError_t status = [] {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, kSplit, kF16, kNT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FwdLayout<D, kNT>::kAlloc);
+    if (e == cudaSuccess) e = check_kernel_regs(fa_fwd_kernel<D, kSplit, kF16, kNT>, kRegsLaunch<kNT>);
+    return e;
+  }();
+  return status;
+}
+
+template <int D, bool kSplit, bool kF16, int kNT>
+cudaError_t launch_fwd_kernel(const FwdParams &p, cudaStream_t stream) {
+  const cudaError_t e = configure_fwd<D, kSplit, kF16, kNT>();
+  if (e != cudaSuccess) return e;
+  const int units = kNT == 2 ? (p.sh.tq + 1) / 2 : p.sh.tq;
+  const int grid = units * p.sh.bh * (kSplit ? p.n_split : 1);
+  LaunchProbe probe(kKindFwd, stream);
+  fa_fwd_kernel<D, kSplit, kF16, kNT>
+      <<<grid, kThreadsFor<kNT>, FwdLayout<D, kNT>::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// d = 64 without the key split: one Q tile per CTA (two CTAs per SM) under a
+// block mask, where a pair of Q tiles walks the union of its two tile lists
+// and often has one tile idle, and where the pairs would fill at most four
+// waves of the GPU, whose CTAs' set-up and epilogue then overlap the other
+// CTA's steps; pairs otherwise (measured at B4 H16 N4096: dense 8 % and causal
+// 1.5 % faster with pairs; block-sparse N8192 19 % and B8 H12 N1024 causal
+// 10 % faster with one tile).
+bool fwd_one_tile(const FwdParams &p) {
+  if (p.q_tiles) return p.q_tiles == 1;
+  if (p.sh.mask) return true;
+  const long long pairs = (long long)((p.sh.tq + 1) / 2) * p.sh.bh;
+  return p.sms > 0 && pairs <= 4LL * p.sms;
+}
+
 template <int D, bool kF16>
 cudaError_t launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
-  using L = FwdLayout<D>;
-  static bool configured = false;  // attribute set once per process (idempotent anyway)
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, false, kF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_fwd_kernel<D, true, kF16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e == cudaSuccess) e = check_kernel_regs(fa_fwd_kernel<D, false, kF16>, kRegsLaunch);
-    if (e == cudaSuccess) e = check_kernel_regs(fa_fwd_kernel<D, true, kF16>, kRegsLaunch);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int grid = ((p.sh.tq + 1) / 2) * p.sh.bh * p.n_split;
-  {
-    LaunchProbe probe(kKindFwd, stream);
-    if (p.n_split > 1)
-      fa_fwd_kernel<D, true, kF16><<<grid, kThreads, L::kAlloc, stream>>>(p);
-    else
-      fa_fwd_kernel<D, false, kF16><<<grid, kThreads, L::kAlloc, stream>>>(p);
-  }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (p.n_split > 1)
+    e = launch_fwd_kernel<D, true, kF16, 2>(p, stream);
+  else if constexpr (D == 64)
+    e = fwd_one_tile(p) ? launch_fwd_kernel<D, false, kF16, 1>(p, stream)
+                        : launch_fwd_kernel<D, false, kF16, 2>(p, stream);
+  else
+    e = launch_fwd_kernel<D, false, kF16, 2>(p, stream);
   if (e != cudaSuccess || p.n_split == 1) return e;
   return launch_combine<D, kF16>(p, stream);
 }

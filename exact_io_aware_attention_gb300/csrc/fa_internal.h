@@ -100,6 +100,9 @@ struct FwdParams {
   uint32_t debug_flags;               // kDebug* bits (tests of the failure path only)
   uint64_t wait_limit_ns;             // limit of one kernel-side wait
   int head_group;                     // CTA order: heads per group (1..bh), fwd_item_head
+  int q_tiles;                        // d = 64 without a split: Q tiles per CTA, 1 or 2 (0: the
+                                      // launch chooses)
+  int sms;                            // SM count (0: unknown)
 };
 
 struct BwdParams {

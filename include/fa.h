@@ -120,6 +120,11 @@ const char *fa_last_error(void);
  * Forward pass, contiguous [B,H,N,d] tensors, Nq = Nk = N. Reads Q, K, V;
  * writes O (bf16 [B,H,N,d]) and LSE (fp32 [B,H,N]). S and P never reach
  * global memory.
+ *
+ * At d = 64 (without a split over the keys) a CTA holds one or two Q tiles:
+ * one under a block mask and when pairs of tiles would fill at most four
+ * waves of the GPU, two otherwise. The environment variable FA_FWD_Q_TILES=1
+ * or 2 fixes the choice (tuning and tests); results agree to rounding order.
  */
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                      int H, int N, int d, int causal, float scale, const uint8_t *block_mask,

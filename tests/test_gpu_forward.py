@@ -49,6 +49,18 @@ def test_forward_small_shapes(N, d, causal):
     full_check(1, 2, N, d, causal, case=100 + N + d, what=f"N={N} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("q_tiles", ["1", "2"])
+@pytest.mark.parametrize("causal,sparse", [(False, False), (True, False), (False, True)])
+def test_forward_d64_q_tiles_per_cta(q_tiles, causal, sparse, monkeypatch):
+    """Both d = 64 forms (one or two Q tiles per CTA, FA_FWD_Q_TILES) against the
+    oracle, with a partial last tile and an odd tile count (a pair with one tile)."""
+    monkeypatch.setenv("FA_FWD_Q_TILES", q_tiles)
+    N = 5 * 128 - 37
+    mask = gen.block_mask((N + 127) // 128, 0.5, seed=907) if sparse else None
+    full_check(1, 3, N, 64, causal, case=910 + int(q_tiles), mask=mask,
+               what=f"q_tiles={q_tiles} causal={causal} sparse={sparse}")
+
+
 def test_forward_single_head_n256_d64():
     """The single-head workload B=1, H=1, N=256, d=64, non-causal, checked in full."""
     w = gen.WORKLOADS["single_head_n256_d64"]
