@@ -55,8 +55,9 @@
 // it (dP^T(n) has already), and the slot takes dO_{n+2} once dK(n) and dQ(n)
 // have read dS^T(n); at d = 64 it has a tile of its own.
 // MMA order per step n: dV(n) (two halves, as P^T(n) arrives), S^T(n+1),
-// dQ(n), dK(n), dP^T(n+1). MMAs issued by one thread execute in issue order,
-// so S^T(n+1) overwrites P^T(n) only after dV(n) has read it.
+// then at d = 64 dP^T(n+1), dQ(n), dK(n), and at d = 96 (dQ in dP^T's
+// columns) dQ(n), dK(n), dP^T(n+1). MMAs issued by one thread execute in issue
+// order, so S^T(n+1) overwrites P^T(n) only after dV(n) has read it.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -437,6 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         }
         ok = mbar_wait_inl(bars.ds_full(), n & 1, st, status_code(kKernBwdFused, kRoleMma, 5));
         if (!ok) break;
+        tc_fence_after();
+        // d = 64 (dQ has columns of its own): dP^T(n+1) goes ahead of dQ(n) and
+        // dK(n), since the softmax warps have read dP^T(n); they form dS^T(n+1)
+        // while dQ(n) and dK(n) run (3 % faster on dense and block-sparse)
+        if (!L::kDqShare && inext < T) {
+          ok = mbar_wait_inl(bars.do_full(ds1), ((n + 1) >> 1) & 1, st,
+                         status_code(kKernBwdFused, kRoleMma, 7));
+          if (!ok) break;
+          tc_fence_after();
+          issue_sq(sV, sdO + ds1 * L::kTileBytes, L::kColDP);
+          mma_commit(bars.dp_full());
+        }
         const int b = L::kDqShare ? 0 : (n & 1);
         if (!L::kDqShare && n >= 2) {  // buffer b was last used by step n - 2
           ok = mbar_wait_inl(bars.dq_free(b), ((n >> 1) - 1) & 1, st,
@@ -452,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
           mma_commit(bars.do_empty(ds));  // dK(n) and dQ(n) have read dS^T(n) in dO_n's slot
         else
           mma_commit(bars.ds_empty());
-        if (inext < T) {
+        if (L::kDqShare && inext < T) {
           if (L::kDqShare) {  // dP^T(n+1) goes where dQ(n) is until it has been read
             ok = mbar_wait_inl(bars.dq_free(0), n & 1, st, status_code(kKernBwdFused, kRoleMma, 10));
             if (!ok) break;
