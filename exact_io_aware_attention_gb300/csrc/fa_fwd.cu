@@ -137,10 +137,8 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, kNT>;
   static_assert(kNT == 2 || (D == 64 && !kSplit), "one Q tile per CTA: d = 64 only");
-  // d = 64 moves registers between the warpgroups (setmaxnreg, below), and
-  // then every wait and store is inlined
+  // d = 64 moves registers between the warpgroups (setmaxnreg, below)
   constexpr bool kMoveRegs = D == 64;
-  constexpr bool kInline = true;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,9 +297,9 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
   // 168 * 384, the launch's total; one Q tile: 56 + 200 = 2 * 128), which
   // keeps the softmax loop free of spills; at d >= 96 the MMA issuer, with
   // twice the MMAs per step, runs slower with fewer registers and the split is
-  // not made. Every call below is
-  // inlined: an out-of-line call in a kernel with its own register counts is
-  // not compiled.
+  // not made. Every wait and store below is inlined: an out-of-line call in a
+  // kernel with its own register counts is not compiled, and the inlined
+  // waits also measured faster at d >= 96.
   if (warp < 4) {
     if constexpr (kMoveRegs) setmaxnreg_dec<kRegsLoadMma<kNT>>();
     if (warp == 0) {
@@ -314,7 +312,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
           for (int which = 0; which < 2 && ok; ++which, ++pos) {
             const int s = pos % L::kStages;
             const uint32_t u = pos / L::kStages;
-            ok = mbar_wait_t<kInline>(bars.kv_empty(s), (u & 1u) ^ 1u, st, status_code(kKernFwd, kRoleLoad, 1));
+            ok = mbar_wait_inl(bars.kv_empty(s), (u & 1u) ^ 1u, st, status_code(kKernFwd, kRoleLoad, 1));
             if (!ok) break;
             mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
             const CUtensorMap *tm = which ? &p.tm_v : &p.tm_k;
@@ -325,10 +323,10 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
         }
         // teardown: wait (bounded) until every copy issued has landed (the Q
         // tiles were loaded during set-up)
-        mbar_wait_drain_t<kInline>(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
+        mbar_wait_drain_inl(bars.q_full(), 0, st, status_code(kKernFwd, kRoleLoad, 2));
         for (int s = 0; s < L::kStages && s < pos; ++s) {
           const int last = s + ((pos - 1 - s) / L::kStages) * L::kStages;  // last pos used on s
-          mbar_wait_drain_t<kInline>(bars.kv_full(s), (last / L::kStages) & 1u, st,
+          mbar_wait_drain_inl(bars.kv_full(s), (last / L::kStages) & 1u, st,
                     status_code(kKernFwd, kRoleLoad, 3));
         }
       }
@@ -338,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
       if (elect_one()) {
         constexpr uint32_t kIdS = idesc_f32acc(kTile, kTile, 0, 0, kF16);  // Q K^T, both K-major
         constexpr uint32_t kIdPV = idesc_f32acc(kTile, D, 0, 1, kF16);     // P V, V is MN-major
-        bool ok = count == 0 || mbar_wait_t<kInline>(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
+        bool ok = count == 0 || mbar_wait_inl(bars.q_full(), 0, st, status_code(kKernFwd, kRoleMma, 1));
         uint32_t pcount[2] = {0, 0};
         bool first_pv[2] = {true, true};
         // d = 64: P_t has tensor-memory columns of its own, so S_t(n+1) waits
@@ -376,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
 
         if (ok && count > 0) {
           // prologue: S for the first K tile
-          ok = mbar_wait_t<kInline>(bars.kv_full(0), 0, st, status_code(kKernFwd, kRoleMma, 2));
+          ok = mbar_wait_inl(bars.kv_full(0), 0, st, status_code(kKernFwd, kRoleMma, 2));
           if (ok) {
             tc_fence_after();
             const uint32_t e = list[0];
@@ -395,10 +393,10 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
           const int vslot = vpos % L::kStages, kslot = kpos % L::kStages;
           const bool has_next = n + 1 < count;
           const uint32_t en = has_next ? list[n + 1] : 0u;
-          ok = mbar_wait_t<kInline>(bars.kv_full(vslot), (vpos / L::kStages) & 1u, st,
+          ok = mbar_wait_inl(bars.kv_full(vslot), (vpos / L::kStages) & 1u, st,
                          status_code(kKernFwd, kRoleMma, 3));
           if (ok && has_next)
-            ok = mbar_wait_t<kInline>(bars.kv_full(kslot), (kpos / L::kStages) & 1u, st,
+            ok = mbar_wait_inl(bars.kv_full(kslot), (kpos / L::kStages) & 1u, st,
                            status_code(kKernFwd, kRoleMma, 4));
           if (!ok) break;
           tc_fence_after();
@@ -406,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
             for (int t = 0; t < kNT && ok; ++t) {
               if (!(has_next && entry_act(en, t))) continue;
               // the previous S_t has been read out of its columns
-              ok = mbar_wait_t<kInline>(bars.s_read(t), (s_issued[t] - 1) & 1u, st,
+              ok = mbar_wait_inl(bars.s_read(t), (s_issued[t] - 1) & 1u, st,
                                  status_code(kKernFwd, kRoleMma, 11 + t));
               if (!ok) break;
               tc_fence_after();
@@ -422,13 +420,13 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
               // form the second half of P_t (the split-key instantiation waits
               // for all of P_t on p_full(t, 1))
               if constexpr (!kSplit) {
-                ok = mbar_wait_t<kInline>(bars.p_full(t, 0), pcount[t] & 1u, st,
+                ok = mbar_wait_inl(bars.p_full(t, 0), pcount[t] & 1u, st,
                                status_code(kKernFwd, kRoleMma, 5 + t));
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(t, vslot, first_pv[t], 0);
               }
-              ok = mbar_wait_t<kInline>(bars.p_full(t, 1), pcount[t] & 1u, st,
+              ok = mbar_wait_inl(bars.p_full(t, 1), pcount[t] & 1u, st,
                              status_code(kKernFwd, kRoleMma, 9 + t));
               if (!ok) break;
               ++pcount[t];
@@ -453,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
         }
         // teardown: every MMA this thread issued has completed
         mma_commit(bars.teardown());
-        mbar_wait_drain_t<kInline>(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
+        mbar_wait_drain_inl(bars.teardown(), 0, st, status_code(kKernFwd, kRoleMma, 8));
       }
       __syncwarp();
     }
@@ -476,14 +474,14 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
       for (int n = 0; n < count; ++n) {
         const uint32_t e = list[n];
         if (!entry_act(e, t)) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.s_full(t), scount & 1u, st,
+        ok = __all_sync(0xffffffffu, mbar_wait_inl(bars.s_full(t), scount & 1u, st,
                                                status_code(kKernFwd, kRoleSoftmax, 1 + t)));
         // d = 64: S_t(n) was issued ahead of PV_t(n-1), so its completion no
         // longer implies that PV_t(n-1) has read P_t and written O_t; wait for
         // that before this step rewrites them
         constexpr bool kEarlyS = D == 64 && !kSplit;
         if (kEarlyS && ok && any)
-          ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.pv_done(0) + ((~threadIdx.x & 128u) >> 4),
+          ok = __all_sync(0xffffffffu, mbar_wait_inl(bars.pv_done(0) + ((~threadIdx.x & 128u) >> 4),
                                                      (scount - 1) & 1u, st,
                                                      status_code(kKernFwd, kRoleSoftmax, 4)));
         if (!ok) break;
@@ -585,7 +583,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
       if (ok && any)
         // this warpgroup's o_done(t), its address from threadIdx (an address
         // computed from t here costs the softmax loop registers and spills)
-        ok = __all_sync(0xffffffffu, mbar_wait_t<kInline>(bars.o_done(0) + ((~threadIdx.x & 128u) >> 4), 0, st,
+        ok = __all_sync(0xffffffffu, mbar_wait_inl(bars.o_done(0) + ((~threadIdx.x & 128u) >> 4), 0, st,
                                                status_code(kKernFwd, kRoleSoftmax, 3)));
       // tensor-memory loads are warp-wide; rows past the sequence end store nothing
       const int qrow = qi * kTile + r;  // query row within the head
@@ -604,7 +602,7 @@ __global__ void __launch_bounds__(kThreadsFor<kNT>, kCtasPerSm<kNT>)
           // 16-bit O through this tile's Q buffer, which the MMAs no longer
           // read (any: its Q load has landed, since the MMAs used it; a tile
           // without keys stores its zeros directly below)
-          store_rows_t<kInline, D, kF16>(&p.tm_o, tO, sQ + t * L::kTileBytes, r, qi * kTile, 0, inv_l,
+          store_rows_tma_inl<D, kF16>(&p.tm_o, tO, sQ + t * L::kTileBytes, r, qi * kTile, 0, inv_l,
                                   any, sh.d, sh.nq, bh_e % sh.heads, bh_e / sh.heads);
         } else {
 #pragma unroll

@@ -118,16 +118,6 @@ __device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, Sta
   return mbar_wait_loop(bar, parity, st, code);
 }
 
-// mbar_wait with the loop inlined (kInline) or out of line.
-template <bool kInline>
-__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, StatusSlot st,
-                                            uint32_t code) {
-  if constexpr (kInline)
-    return mbar_wait_inl(bar, parity, st, code);
-  else
-    return mbar_wait(bar, parity, st, code);
-}
-
 // Teardown wait for copies and MMAs this CTA has already issued. Unlike
 // mbar_wait it keeps waiting after another role of the CTA has given up:
 // work in flight still writes this CTA's shared and tensor memory, so the CTA
@@ -149,15 +139,6 @@ __device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parit
 static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, StatusSlot st,
                                                     uint32_t code) {
   return mbar_wait_drain_inl(bar, parity, st, code);
-}
-
-template <bool kInline>
-__device__ __forceinline__ bool mbar_wait_drain_t(uint32_t bar, uint32_t parity, StatusSlot st,
-                                                  uint32_t code) {
-  if constexpr (kInline)
-    return mbar_wait_drain_inl(bar, parity, st, code);
-  else
-    return mbar_wait_drain(bar, parity, st, code);
 }
 
 // Register count of this warp's warpgroup: every warp of a warpgroup runs the

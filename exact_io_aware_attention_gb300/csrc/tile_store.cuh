@@ -76,17 +76,4 @@ __device__ __noinline__ void store_rows_tma(const CUtensorMap *tm, uint32_t tacc
                                   h_idx, b_idx);
 }
 
-// store_rows_tma_inl (kInline) or its out-of-line copy
-template <bool kInline, int kCols, bool kF16>
-__device__ __forceinline__ void store_rows_t(const CUtensorMap *tm, uint32_t tacc, uint32_t s_tile,
-                                             int r, int tile_row0, int x0, float sc, bool any,
-                                             int d_cols, int n_rows, int h_idx, int b_idx) {
-  if constexpr (kInline)
-    store_rows_tma_inl<kCols, kF16>(tm, tacc, s_tile, r, tile_row0, x0, sc, any, d_cols, n_rows,
-                                    h_idx, b_idx);
-  else
-    store_rows_tma<kCols, kF16>(tm, tacc, s_tile, r, tile_row0, x0, sc, any, d_cols, n_rows, h_idx,
-                                b_idx);
-}
-
 }  // namespace fa
