@@ -16,7 +16,9 @@
 // "Experiments & Results") visits only the tiles whose mask byte is set.
 //
 // CTA = one head, two consecutive 128-row Q tiles (t = 0, 1) sharing one
-// stream of K/V tiles. 12 warps:
+// stream of K/V tiles; at d = 64 (without the key split) also one Q tile per
+// CTA with two CTAs per SM (kNT = 1: warps 0-7, 256 tensor-memory columns;
+// the launch chooses, see fwd_one_tile). 12 warps:
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j through a smem ring
 //               (Q and the first K/V tile are issued during set-up)
 //   warp 1      tcgen05 issuer (one lane) and tensor-memory owner
@@ -26,10 +28,12 @@
 //   warps 8-11  softmax of Q tile 1
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S_0   [128,256) S_1   [256,256+d) O_0   [256+d,256+2d) O_1
-//   P_t (16-bit pairs): the first 64 columns of S_t (d = 128) or [384+64t, +64) (d = 64)
+//   P_t (16-bit pairs): the first 64 columns of S_t (d >= 96) or [384+64t, +64) (d = 64)
 // The MMA issue order PV_0(n), S_0(n+1), PV_1(n), S_1(n+1) lets the tensor
-// core work on one Q tile while the other tile's softmax runs. Each Q tile's
-// epilogue starts once its own last PV has completed (o_done[t]).
+// core work on one Q tile while the other tile's softmax runs; at d = 64,
+// where P_t has columns of its own, S_t(n+1) goes out once the softmax warps
+// have read S_t(n), ahead of PV_t(n). Each Q tile's epilogue starts once its
+// own last PV has completed (o_done[t]).
 //
 // Split over the keys (few Q tiles, many keys, e.g. decoding against a long
 // cache): n_split CTAs share one Q-tile pair, each taking a contiguous share
