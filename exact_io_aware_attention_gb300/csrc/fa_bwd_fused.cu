@@ -95,7 +95,7 @@ struct FusedLayout {
   static_assert(!kList || D == 64, "Q-tile list: d = 64 only");
   static constexpr int kListOff = kDeltaOff + kdOSlots * kTile * 4;
   static constexpr int kBarOff = kListOff + (kQList ? kMaxTiles * 2 : 0);
-  static constexpr int kNumBars = 24;
+  static constexpr int kNumBars = 26;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -125,6 +125,8 @@ struct Bars {
   __device__ uint32_t dq_full(int b) const { return base + 8 * (17 + b); }
   __device__ uint32_t dq_free(int b) const { return base + 8 * (19 + b); }
   __device__ uint32_t acc_done() const { return base + 8 * 21; }
+  __device__ uint32_t dv_done() const { return base + 8 * 24; }
+  __device__ uint32_t dk_done() const { return base + 8 * 25; }
   __device__ uint32_t teardown() const { return base + 8 * 22; }
 };
 
@@ -199,6 +201,10 @@ __device__ __forceinline__ void load_do(const BwdParams &p, const Bars &bars, in
 template <int D, bool kF16, bool kList>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constant__ BwdParams p) {
   using L = FusedLayout<D, kList>;
+  // d = 64: the epilogue stores dV once its last product has completed and
+  // dK once its own has (issued ahead of the last dQ), staged through V's
+  // buffer and a dO slot, which no MMA reads by then
+  constexpr bool kEarlyEpi = !L::kDsInDo && !L::kDqShare;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);  // [0] tmem [2] abort [3] list length
@@ -264,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
       mbar_init(bars.dq_free(b), 128);
     }
     mbar_init(bars.acc_done(), 1);
+    mbar_init(bars.dv_done(), 1);
+    mbar_init(bars.dk_done(), 1);
     mbar_init(bars.teardown(), 1);
     misc[2] = 0;
     fence_mbar_init();
@@ -425,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         if (!ok) break;
         tc_fence_after();
         issue_dv(sdO + ds * L::kTileBytes, n == 0, 1);
+        if (kEarlyEpi && inext >= T) mma_commit(bars.dv_done());
         if (L::kDsInDo)
           mma_commit(bars.dv_step());  // dV(n) has read dO_n: dS^T(n) may go there
         else
@@ -451,6 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
           mma_commit(bars.dp_full());
         }
         const int b = L::kDqShare ? 0 : (n & 1);
+        // d = 64, the item's last step: dK ahead of dQ, so that the epilogue
+        // need not wait for the last dQ
+        const bool dk_first = kEarlyEpi && inext >= T;
+        if (dk_first) {
+          issue_dk(ds_tile(n), sQ + qs * L::kTileBytes, n == 0);
+          mma_commit(bars.q_empty(qs));
+          mma_commit(bars.dk_done());
+        }
         if (!L::kDqShare && n >= 2) {  // buffer b was last used by step n - 2
           ok = mbar_wait_inl(bars.dq_free(b), ((n >> 1) - 1) & 1, st,
                          status_code(kKernBwdFused, kRoleMma, 9));
@@ -459,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
         tc_fence_after();
         issue_dq(ds_tile(n), b ? L::kColDQ1 : L::kColDQ0);
         mma_commit(bars.dq_full(b));
-        issue_dk(ds_tile(n), sQ + qs * L::kTileBytes, n == 0);
-        mma_commit(bars.q_empty(qs));
+        if (!dk_first) {
+          issue_dk(ds_tile(n), sQ + qs * L::kTileBytes, n == 0);
+          mma_commit(bars.q_empty(qs));
+        }
         if (L::kDsInDo)
           mma_commit(bars.do_empty(ds));  // dK(n) and dQ(n) have read dS^T(n) in dO_n's slot
         else
@@ -581,16 +600,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_fused(const __grid_constan
       mbar_arrive(bars.ds_full());
       mbar_arrive(bars.do_empty(ds));  // D_i has been read
     }
-    // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled), through the
-    // K_j and V_j buffers, which no MMA reads once every MMA has completed
+    // epilogue: warps 4-7 write dV, warps 8-11 write dK (scaled); at d = 96
+    // through the K_j and V_j buffers once every MMA has completed, at d = 64
+    // each as soon as its own last product has (V's buffer and dO slot 0)
     if (ok && any)
-      ok = __all_sync(0xffffffffu, mbar_wait_inl(bars.acc_done(), 0, st,
+      ok = __all_sync(0xffffffffu, mbar_wait_inl(kEarlyEpi ? (h ? bars.dk_done() : bars.dv_done())
+                                                           : bars.acc_done(), 0, st,
                                              status_code(kKernBwdFused, kRoleSoftmax, 6)));
     if (ok) {
       tc_fence_after();
       store_rows_tma_inl<D, kF16>(h ? &p.tm_dk : &p.tm_dv, t + (h ? L::kColDK : L::kColDV),
-                              h ? sV : sK, kr, j * kTile, 0, h ? p.scale : 1.f, any, sh.d, sh.nk,
-                              h_idx, b_idx);
+                              kEarlyEpi ? (h ? sdO : sV) : (h ? sV : sK), kr, j * kTile, 0,
+                              h ? p.scale : 1.f, any, sh.d, sh.nk, h_idx, b_idx);
     }
   } else {
     setmaxnreg_dec<104>();
