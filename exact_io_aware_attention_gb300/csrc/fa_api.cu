@@ -166,13 +166,29 @@ bool encode_dq_acc(CUtensorMap *m, float *base, long long rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
-// Heads per CTA group of the backward grid (kept small so the fp32 dQ rows
-// that concurrent CTAs accumulate stay in L2). FA_BWD_HEAD_GROUP overrides it
-// for tuning runs.
-int backward_head_group(int bh) {
+int sm_count();
+
+// Heads per CTA group of the backward grid, whose CTAs run heavy K/V tiles
+// first within each group. Groups are kept small so that the fp32 dQ rows
+// the CTAs in flight accumulate stay in L2: 8 heads. With at most 8 K/V tiles
+// per head (N <= 1024) a group of 8 holds less than half a wave of CTAs and
+// the heavy-first order no longer balances the SMs, so a group holds two
+// waves there (measured at N = 1024, d = 64 and 128: 2-5 % faster than 8;
+// the dQ rows in flight stay near 2 * SMs * 128). Longer sequences keep 8:
+// at N = 4096, groups of 8 and 16 measured level and 10 measured 4.7 %
+// slower. FA_BWD_HEAD_GROUP overrides it for tuning runs.
+int backward_head_group(int bh, int tk) {
   const char *e = getenv("FA_BWD_HEAD_GROUP");
   const int from_env = e ? atoi(e) : 0;
-  const int g = from_env > 0 ? from_env : 8;
+  int g = from_env;
+  if (g <= 0) {
+    const int sms = sm_count();
+    g = 8;
+    if (tk > 0 && tk <= 8 && sms > 0) {
+      const int two_waves = (2 * sms + tk - 1) / tk;
+      if (two_waves > g) g = two_waves;
+    }
+  }
   return g < bh ? g : bh;
 }
 
@@ -453,7 +469,7 @@ fa_status backward_impl(const fa_tensor *Q, const fa_tensor *K, const fa_tensor 
   p.dv = dV->data;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.head_group = backward_head_group(p.sh.bh);
+  p.head_group = backward_head_group(p.sh.bh, p.sh.tk);
   p.debug_flags = g_debug_flags.load();
   p.wait_limit_ns = g_wait_limit_ns.load() ? g_wait_limit_ns.load() : fa::kWaitLimitNs;
   cudaError_t e = status_word(&p.status);
