@@ -316,12 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
         for (int x = 0; x < kTile; ++x)
           if (x >= lim) s[x] = -INFINITY;
       }
+      // row max: 4 independent partial maxima, two new keys per three-input max
       float mp[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) mp[x] = s[x];
+      for (int y = 0; y < 4; ++y) mp[y] = fmaxf(s[2 * y], s[2 * y + 1]);
 #pragma unroll
-      for (int x = 4; x < kTile; ++x) mp[x & 3] = fmaxf(mp[x & 3], s[x]);
-      const float m_tile = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])) * c;
+      for (int x = 8; x < kTile; x += 8)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) mp[y] = fmax3(mp[y], s[x + 2 * y], s[x + 2 * y + 1]);
+      const float m_tile = fmax3(mp[0], mp[1], fmaxf(mp[2], mp[3])) * c;
       const bool need = m_tile > m_used + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
@@ -329,26 +332,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
         m_used = m_tile;
       }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(s*c - m), the scaling and the row sum on packed fp32 pairs
+      // (one instruction per two keys; the sum in 4 partial sums)
+      const uint64_t c2 = f2pack(c, c), nm2 = f2pack(-m_sub, -m_sub);
+      uint64_t lp2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
       uint32_t pk0[32], pk1[32];
+      auto p_pair = [&](int x, float s0, float s1) {
+        float p0, p1;
+        f2unpack(ffma2(f2pack(s0, s1), c2, nm2), p0, p1);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        lp2[x & 1] = fadd2(lp2[x & 1], f2pack(p0, p1));
+        return pack2<kF16>(p0, p1);
+      };
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const float p0 = ex2_approx(fmaf(s[2 * x], c, -m_sub));
-        const float p1 = ex2_approx(fmaf(s[2 * x + 1], c, -m_sub));
-        lp[x & 3] += p0 + p1;
-        pk0[x] = pack2<kF16>(p0, p1);
-      }
+      for (int x = 0; x < 32; ++x) pk0[x] = p_pair(x, s[2 * x], s[2 * x + 1]);
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const float p0 = ex2_approx(fmaf(s[64 + 2 * x], c, -m_sub));
-        const float p1 = ex2_approx(fmaf(s[64 + 2 * x + 1], c, -m_sub));
-        lp[x & 3] += p0 + p1;
-        pk1[x] = pack2<kF16>(p0, p1);
-      }
+      for (int x = 0; x < 32; ++x) pk1[x] = p_pair(x, s[64 + 2 * x], s[64 + 2 * x + 1]);
+      float lp[2];
+      f2unpack(fadd2(lp2[0], lp2[1]), lp[0], lp[1]);
       // P into the first 64 columns of this S buffer
       tmem_st32(tS, pk0);
       tmem_st32(tS + 32, pk1);
-      l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+      l = l * alpha + (lp[0] + lp[1]);
       if (n > 0 && __any_sync(0xffffffffu, need)) {
         // O *= alpha for this row, once PV(n-1) has completed (PV(n) cannot
         // have: it needs this P)
